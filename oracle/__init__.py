@@ -1,0 +1,173 @@
+"""fp64 CPU oracle for dynamic-mask sparse attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never calls it, and
+it shares no code with the CUDA path: the arithmetic lives in ``dma_oracle.c``
+(plain C, fp64, OpenMP over independent (batch, head) segments), compiled by
+``build()`` with gcc and loaded through ctypes.
+
+Functions (all take CPU torch tensors; floating inputs are widened to fp32
+exactly -- bf16 is a subset of fp32 -- and every result is fp64):
+
+* ``score(V, W, A)``            importance s = A_h * softplus(v . w_h)
+* ``select(scores, w, ...)``    per-key top-set interval end ("expiry")
+* ``attend_rows(...)``          dense masked softmax attention for listed rows
+* ``decode(...)``               the last row of a cache of length L
+* ``kept_set(...)``             the kept key set of one row, from an expiry array
+
+Method source: Dynamic Mask Attention summary (lsdiaocha.cn), §四 and §五.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dma_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+ROWWISE = 0
+GLOBAL = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp64, no fast-math) into oracle/liboracle.so."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-Wall", "-o", tmp, _SRC,
+                               "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.oracle_score.argtypes = [P, P, P, I, I, I, I, I, I, P]
+        lib.oracle_select.argtypes = [P, I, I, I, I, I, I, P]
+        lib.oracle_attend_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, P, P]
+        lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P]
+        lib.oracle_num_threads.restype = I
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def _f32(t: torch.Tensor) -> np.ndarray:
+    return np.ascontiguousarray(t.detach().to("cpu", torch.float32).numpy())
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def score(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor] = None, key_begin: int = 0,
+          key_end: Optional[int] = None) -> torch.Tensor:
+    """s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>), fp64 [B][Hkv][S].
+
+    Keys outside [key_begin, key_end) are left at 0.
+    """
+    B, S, Hkv, D = V.shape
+    key_end = S if key_end is None else key_end
+    v, w = _f32(V), _f32(W)
+    a = None if A is None else _f32(A)
+    out = np.zeros((B, Hkv, S), dtype=np.float64)
+    _load().oracle_score(_ptr(v), _ptr(w), _ptr(a), B, S, Hkv, D, key_begin, key_end, _ptr(out))
+    return torch.from_numpy(out)
+
+
+def select(scores: torch.Tensor, w: int, block: int = 1, mode: int = ROWWISE) -> torch.Tensor:
+    """Per-key top-set interval end ("expiry"), int32 [B][Hkv][S].
+
+    Key j is in the top set of rows lo_j <= i < expiry_j (lo_j = j for tokens,
+    the block's last key for blocks); expiry_j = min(lo_j, S) means never.
+    """
+    B, Hkv, S = scores.shape
+    s = np.ascontiguousarray(scores.to(torch.float64).numpy())
+    out = np.zeros((B, Hkv, S), dtype=np.int32)
+    _load().oracle_select(_ptr(s), B, Hkv, S, w, block, mode, _ptr(out))
+    return torch.from_numpy(out)
+
+
+def attend_rows(Q, K, V, scores, expiry, rows: Sequence[int], window: int, block: int = 1,
+                scale: Optional[float] = None):
+    """Dense masked softmax attention for the listed rows of every (b, hq).
+
+    Returns (O [B][n_rows][H][D], lse [B][H][n_rows]) in fp64.
+    """
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    q, k, v = _f32(Q), _f32(K), _f32(V)
+    s = np.ascontiguousarray(scores.to(torch.float64).numpy())
+    e = np.ascontiguousarray(expiry.to(torch.int32).numpy())
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    O = np.zeros((B, len(r), H, D), dtype=np.float64)
+    lse = np.zeros((B, H, len(r)), dtype=np.float64)
+    _load().oracle_attend_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(e), B, S, H, Hkv, D, window, block,
+                               float(scale), len(r), _ptr(r), _ptr(O), _ptr(lse))
+    return torch.from_numpy(O), torch.from_numpy(lse)
+
+
+def prefill(Q, K, V, W, A, w: int, window: int, block: int = 1, mode: int = ROWWISE, rows=None, scale=None):
+    """Score, select and attend in one call.  Returns (O, lse, scores, expiry)."""
+    S = Q.shape[1]
+    sc = score(V, W, A)
+    ex = select(sc, w, block, mode)
+    rows = list(range(S)) if rows is None else rows
+    O, lse = attend_rows(Q, K, V, sc, ex, rows, window, block, scale)
+    return O, lse, sc, ex
+
+
+def decode(q, Kc, Vc, cache_len, scores, w: int, window: int, block: int = 1, mode: int = ROWWISE, scale=None):
+    """Attention of one new query row per sequence over its cache of length
+    cache_len[b].  q [B][H][D]; Kc, Vc [B][Lmax][Hkv][D]; scores fp64
+    [B][Hkv][Lmax].  Returns (o [B][H][D], lse [B][H]) in fp64."""
+    B, H, D = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    qq, k, v = _f32(q), _f32(Kc), _f32(Vc)
+    cl = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int32))
+    s = np.ascontiguousarray(scores.to(torch.float64).numpy())
+    o = np.zeros((B, H, D), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    _load().oracle_decode(_ptr(qq), _ptr(k), _ptr(v), _ptr(cl), _ptr(s), B, Lmax, H, Hkv, D, w, window, block,
+                          mode, float(scale), _ptr(o), _ptr(lse))
+    return torch.from_numpy(o), torch.from_numpy(lse)
+
+
+def top_lo(j, block: int):
+    """First row at which key j may enter the top set (its block's last key)."""
+    if block <= 1:
+        return j
+    return (j // block) * block + block - 1
+
+
+def kept_set(expiry_seg: torch.Tensor, i: int, window: int, block: int = 1) -> set:
+    """Kept keys of row i for one (b, h) segment: top interval or local window."""
+    ex = expiry_seg.tolist()
+    out = set()
+    for j in range(i + 1):
+        if j > i - window or (top_lo(j, block) <= i < ex[j]):
+            out.add(j)
+    return out
+
+
+def top_set(expiry_seg: torch.Tensor, i: int, block: int = 1) -> set:
+    """Top-set keys of row i (no window) for one (b, h) segment."""
+    ex = expiry_seg.tolist()
+    return {j for j in range(i + 1) if top_lo(j, block) <= i < ex[j]}
