@@ -1,0 +1,296 @@
+"""Dynamic-mask sparse attention on B300 (sm_103a): Python binding of libdma.
+
+This module only marshals arguments into the C ABI declared in
+``include/dma.h``; every step of the computation runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  If ``libdma.so`` is not
+built, importing this package raises ImportError: there is no fallback.
+
+The functions carry the C names:
+
+* ``dma_score_keys``          s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>)
+* ``dma_select_topk``         causal top-w selection (FULL or UPDATE)
+* ``dma_sparse_attn_prefill`` masked softmax attention over the kept keys
+* ``dma_sparse_attn_decode``  the same for one new query row per sequence
+
+plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and two
+compositions, ``prefill`` and ``DecodeState``, for the common call sequences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdma.so")
+
+DMA_OK = 0
+DMA_ERR_INVALID_ARG = 1
+DMA_ERR_UNSUPPORTED = 2
+DMA_ERR_WORKSPACE = 3
+DMA_ERR_CUDA = 4
+DMA_ERR_TIMEOUT = 5
+DMA_ERR_DEVICE_CHECK = 6
+
+DMA_F32 = 0
+DMA_BF16 = 1
+ROWWISE = 0
+GLOBAL = 1
+FULL = 0
+UPDATE = 1
+Q_TILE = 128
+
+
+class DmaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (_status_name(status), msg))
+        self.status = status
+
+
+class KeptT(ctypes.Structure):
+    """Mirror of dma_kept_t (include/dma.h)."""
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("B", "Hkv", "S", "w", "window", "block", "mode", "q_tile", "n_qt", "cap", "top_cap",
+                 "tile_stride", "bitmap_words")] + \
+               [(n, ctypes.c_void_p) for n in
+                ("expiry", "idx", "count", "top_idx", "top_count", "tile_cnt", "tile_idx", "bitmap")]
+
+
+EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_attn_prefill",
+            "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_get_device_status", "dma_status_string",
+            "dma_last_error_message", "dma_set_prefill_kernel", "dma_version")
+
+
+def _load_lib():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libdma.so is not built (%s); run: python -m content_aware_dynamic_dma_b300.build" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    PK = ctypes.POINTER(KeptT)
+    sig = {
+        "dma_score_keys": [P, I, I, I, I, I, I, I, P, P, P, P],
+        "dma_kept_layout": [I, I, I, I, I, I, I, PK, ctypes.POINTER(Z)],
+        "dma_select_topk": [P, I, I, I, I, I, I, I, I, P, PK, P, Z, P],
+        "dma_sparse_attn_prefill": [P, P, P, I, I, I, I, I, I, P, PK, F, P, P, P],
+        "dma_decode_workspace_size": [I, I, I, I, I, I, ctypes.POINTER(Z)],
+        "dma_sparse_attn_decode": [P, P, P, I, I, I, P, I, I, I, P, PK, F, P, P, P, Z, P],
+        "dma_get_device_status": [P, ctypes.POINTER(I)],
+        "dma_status_string": [I],
+        "dma_last_error_message": [],
+        "dma_set_prefill_kernel": [I],
+        "dma_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = I
+    lib.dma_status_string.restype = ctypes.c_char_p
+    lib.dma_last_error_message.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load_lib()
+
+
+def _status_name(s: int) -> str:
+    return _lib.dma_status_string(s).decode()
+
+
+def _check(status: int):
+    if status != DMA_OK:
+        raise DmaError(status, _lib.dma_last_error_message().decode())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return DMA_F32
+    if t.dtype == torch.bfloat16:
+        return DMA_BF16
+    raise TypeError("tensor dtype %s: expected float32 or bfloat16" % t.dtype)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- C names ----
+
+def dma_score_keys(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor], scores: torch.Tensor,
+                   key_begin: int = 0, key_end: Optional[int] = None, stream=None) -> None:
+    B, S, Hkv, D = V.shape
+    key_end = S if key_end is None else key_end
+    _check(_lib.dma_score_keys(_ptr(V), _dtype(V), B, S, Hkv, D, key_begin, key_end, _ptr(W), _ptr(A), _ptr(scores),
+                               _stream(stream)))
+
+
+def dma_kept_layout(B: int, Hkv: int, S: int, w: int, window: int, block: int = 1, mode: int = ROWWISE):
+    k = KeptT()
+    ws = ctypes.c_size_t(0)
+    _check(_lib.dma_kept_layout(B, Hkv, S, w, window, block, mode, ctypes.byref(k), ctypes.byref(ws)))
+    return k, ws.value
+
+
+class Kept:
+    """Caller-owned kept-key arrays (torch device tensors) and their dma_kept_t."""
+
+    def __init__(self, B: int, Hkv: int, S: int, w: int, window: int, block: int = 1, mode: int = ROWWISE,
+                 device="cuda", tiles: bool = True, top: bool = True, bitmap: bool = True):
+        self.t, self.select_ws_bytes = dma_kept_layout(B, Hkv, S, w, window, block, mode)
+        t = self.t
+        i32 = dict(dtype=torch.int32, device=device)
+        self.expiry = torch.empty((B, Hkv, S), **i32)
+        self.idx = torch.empty((B, Hkv, t.cap), **i32)
+        self.count = torch.zeros((B, Hkv), **i32)
+        self.top_idx = torch.empty((B, Hkv, t.top_cap), **i32) if top else None
+        self.top_count = torch.zeros((B, Hkv), **i32) if top else None
+        self.tile_cnt = torch.zeros((B, Hkv, t.n_qt), **i32) if tiles else None
+        self.tile_idx = torch.empty((B, Hkv, t.n_qt, t.tile_stride), **i32) if tiles else None
+        self.bitmap = (torch.zeros((B, Hkv, t.n_qt, t.bitmap_words), dtype=torch.int32, device=device)
+                       if (tiles and bitmap) else None)
+        self.ws = torch.empty((max(self.select_ws_bytes, 16),), dtype=torch.uint8, device=device)
+        for name in ("expiry", "idx", "count", "top_idx", "top_count", "tile_cnt", "tile_idx", "bitmap"):
+            ten = getattr(self, name)
+            setattr(t, name, ten.data_ptr() if ten is not None else None)
+
+    @property
+    def B(self):
+        return self.t.B
+
+    @property
+    def Hkv(self):
+        return self.t.Hkv
+
+    @property
+    def S(self):
+        return self.t.S
+
+    @property
+    def w(self):
+        return self.t.w
+
+    @property
+    def window(self):
+        return self.t.window
+
+    @property
+    def block(self):
+        return self.t.block
+
+    @property
+    def mode(self):
+        return self.t.mode
+
+
+def dma_select_topk(scores: torch.Tensor, kept: Kept, op: int = FULL, seq_len: Optional[torch.Tensor] = None,
+                    ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    B, Hkv, S = scores.shape
+    t = kept.t
+    ws = kept.ws if ws is None else ws
+    _check(_lib.dma_select_topk(_ptr(scores), B, Hkv, S, t.w, t.window, t.block, t.mode, op, _ptr(seq_len),
+                                ctypes.byref(t), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dma_sparse_attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scores: torch.Tensor, kept: Kept,
+                            O: torch.Tensor, lse: Optional[torch.Tensor] = None, scale: float = 0.0,
+                            stream=None) -> None:
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    _check(_lib.dma_sparse_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _dtype(Q), B, S, H, Hkv, D, _ptr(scores),
+                                        ctypes.byref(kept.t), float(scale), _ptr(O), _ptr(lse), _stream(stream)))
+
+
+def dma_decode_workspace_size(B: int, H: int, Hkv: int, D: int, top_cap: int, window: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.dma_decode_workspace_size(B, H, Hkv, D, top_cap, window, ctypes.byref(n)))
+    return n.value
+
+
+def dma_sparse_attn_decode(q: torch.Tensor, Kc: torch.Tensor, Vc: torch.Tensor, scores: torch.Tensor, kept: Kept,
+                           o: torch.Tensor, ws: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                           cache_len: Optional[torch.Tensor] = None, scale: float = 0.0, stream=None) -> None:
+    B, H, D = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    _check(_lib.dma_sparse_attn_decode(_ptr(q), _ptr(Kc), _ptr(Vc), _dtype(q), B, Lmax, _ptr(cache_len), H, Hkv, D,
+                                       _ptr(scores), ctypes.byref(kept.t), float(scale), _ptr(o), _ptr(lse),
+                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dma_get_device_status(stream=None) -> int:
+    v = ctypes.c_int(0)
+    _check(_lib.dma_get_device_status(_stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+def dma_set_prefill_kernel(which: int) -> int:
+    """0 = automatic (tensor-core kernel for bf16), 1 = SIMT kernel."""
+    return _lib.dma_set_prefill_kernel(which)
+
+
+def dma_version() -> int:
+    return _lib.dma_version()
+
+
+# ------------------------------------------------------------ compositions ---
+
+def prefill(Q, K, V, W, A, w: int, window: int, block: int = 1, mode: int = ROWWISE, scale: float = 0.0,
+            kept: Optional[Kept] = None, with_lse: bool = True, stream=None):
+    """Score, select and attend: the whole prefill hot path in three library calls.
+
+    Returns (O, lse, scores, kept)."""
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=Q.device)
+    dma_score_keys(V, W, A, scores, stream=stream)
+    if kept is None:
+        kept = Kept(B, Hkv, S, w, window, block, mode, device=Q.device)
+    dma_select_topk(scores, kept, FULL, stream=stream)
+    O = torch.empty_like(Q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=Q.device) if with_lse else None
+    dma_sparse_attn_prefill(Q, K, V, scores, kept, O, lse, scale, stream=stream)
+    return O, lse, scores, kept
+
+
+class DecodeState:
+    """Decode-side buffers: the score cache, the kept top set and the workspace."""
+
+    def __init__(self, B: int, Lmax: int, H: int, Hkv: int, D: int, w: int, window: int, device="cuda"):
+        self.B, self.Lmax, self.H, self.Hkv, self.D = B, Lmax, H, Hkv, D
+        self.scores = torch.zeros((B, Hkv, Lmax), dtype=torch.float32, device=device)
+        self.kept = Kept(B, Hkv, Lmax, w, window, 1, ROWWISE, device=device, tiles=False)
+        self.ws = torch.empty((dma_decode_workspace_size(B, H, Hkv, D, self.kept.t.top_cap, window),),
+                              dtype=torch.uint8, device=device)
+
+    def full_select(self, Kc, Vc, W, A=None, length: Optional[int] = None, stream=None):
+        """Scores the first ``length`` cache rows and selects the top set of row length-1."""
+        length = self.Lmax if length is None else length
+        dma_score_keys(Vc, W, A, self.scores, 0, length, stream=stream)
+        if length == self.Lmax:
+            dma_select_topk(self.scores, self.kept, FULL, stream=stream)
+            return
+        sub = Kept(self.B, self.Hkv, length, self.kept.w, self.kept.window, 1, ROWWISE, device=self.scores.device,
+                   tiles=False)
+        sc = self.scores[:, :, :length].contiguous()
+        dma_select_topk(sc, sub, FULL, stream=stream)
+        self.kept.top_idx[:, :, :sub.t.top_cap].copy_(sub.top_idx)
+        self.kept.top_count.copy_(sub.top_count)
+
+    def step(self, q, Kc, Vc, W, cache_len: torch.Tensor, new_pos: int, o, lse=None, A=None, scale: float = 0.0,
+             stream=None):
+        """One decode step for a token already appended at ``new_pos`` (= cache_len - 1)."""
+        dma_score_keys(Vc, W, A, self.scores, new_pos, new_pos + 1, stream=stream)
+        dma_select_topk(self.scores, self.kept, UPDATE, seq_len=cache_len, stream=stream)
+        dma_sparse_attn_decode(q, Kc, Vc, self.scores, self.kept, o, self.ws, lse, cache_len, scale, stream=stream)

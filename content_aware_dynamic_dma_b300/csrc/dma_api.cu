@@ -1,0 +1,297 @@
+// C ABI of libdma: argument validation, error reporting and kernel dispatch.
+// Every entry point checks its arguments completely before it enqueues any
+// work, so an argument error never leaves a partial launch behind.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "dma_internal.cuh"
+
+namespace dma {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+// Device status word: kernels record conditions they find (a bounded wait that
+// ran out, an internal capacity check) here; dma_get_device_status reads and
+// clears it.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+int g_prefill_kernel = 0;  // 0 automatic, 1 SIMT
+
+dma_status_t fail(dma_status_t s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+dma_status_t ok()
+{
+    g_msg[0] = '\0';
+    return DMA_OK;
+}
+
+dma_status_t cuda_fail(cudaError_t e, const char* where)
+{
+    return fail(DMA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Address of the status word on the current device (looked up once per device).
+dma_status_t status_ptr(int** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DMA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return DMA_OK;
+}
+
+dma_status_t check_common(dma_dtype_t dt, int B, int S, int Hkv, int D)
+{
+    if (dt != DMA_F32 && dt != DMA_BF16) return fail(DMA_ERR_INVALID_ARG, "dtype %d is neither DMA_F32 nor DMA_BF16", (int)dt);
+    if (B < 1 || S < 1 || Hkv < 1) return fail(DMA_ERR_INVALID_ARG, "B=%d S=%d Hkv=%d must be >= 1", B, S, Hkv);
+    if (D != 64 && D != 128) return fail(DMA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+    if ((int64_t)B * S * Hkv * D > ((int64_t)1 << 40)) return fail(DMA_ERR_UNSUPPORTED, "tensor too large");
+    return DMA_OK;
+}
+
+int64_t kept_top_budget(int w, int S, int block)
+{
+    int64_t k = block <= 1 ? w : (int64_t)(w / block) * block;
+    return k < S ? k : S;
+}
+
+dma_status_t check_kept_geometry(const dma_kept_t* kept, int B, int Hkv, int S)
+{
+    if (!kept) return fail(DMA_ERR_INVALID_ARG, "kept is NULL");
+    if (kept->B != B || kept->Hkv != Hkv || kept->S != S)
+        return fail(DMA_ERR_INVALID_ARG, "kept layout (B=%d Hkv=%d S=%d) does not match the call (B=%d Hkv=%d S=%d)",
+                    kept->B, kept->Hkv, kept->S, B, Hkv, S);
+    dma_kept_t ref{};
+    size_t ws = 0;
+    dma_status_t s = dma_kept_layout(kept->B, kept->Hkv, kept->S, kept->w, kept->window, kept->block,
+                                     (dma_sel_mode_t)kept->mode, &ref, &ws);
+    if (s != DMA_OK) return s;
+    if (ref.q_tile != kept->q_tile || ref.n_qt != kept->n_qt || ref.cap != kept->cap || ref.top_cap != kept->top_cap ||
+        ref.tile_stride != kept->tile_stride || ref.bitmap_words != kept->bitmap_words)
+        return fail(DMA_ERR_INVALID_ARG, "kept geometry was not produced by dma_kept_layout for these sizes");
+    return DMA_OK;
+}
+
+}  // namespace
+}  // namespace dma
+
+using namespace dma;
+
+extern "C" {
+
+int dma_version(void) { return 1; }
+
+const char* dma_status_string(dma_status_t s)
+{
+    switch (s) {
+    case DMA_OK: return "DMA_OK";
+    case DMA_ERR_INVALID_ARG: return "DMA_ERR_INVALID_ARG";
+    case DMA_ERR_UNSUPPORTED: return "DMA_ERR_UNSUPPORTED";
+    case DMA_ERR_WORKSPACE: return "DMA_ERR_WORKSPACE";
+    case DMA_ERR_CUDA: return "DMA_ERR_CUDA";
+    case DMA_ERR_TIMEOUT: return "DMA_ERR_TIMEOUT";
+    case DMA_ERR_DEVICE_CHECK: return "DMA_ERR_DEVICE_CHECK";
+    }
+    return "DMA_ERR_UNKNOWN";
+}
+
+const char* dma_last_error_message(void) { return g_msg; }
+
+int dma_set_prefill_kernel(int which)
+{
+    int old = g_prefill_kernel;
+    g_prefill_kernel = which;
+    return old;
+}
+
+dma_status_t dma_get_device_status(dma_stream_t stream, int* device_status)
+{
+    if (!device_status) return fail(DMA_ERR_INVALID_ARG, "device_status is NULL");
+    int* p = nullptr;
+    dma_status_t s = status_ptr(&p);
+    if (s != DMA_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+    *device_status = v;
+    return ok();
+}
+
+dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
+                            const float* W, const float* A, float* scores, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (!V || !W || !scores) return fail(DMA_ERR_INVALID_ARG, "V, W and scores must be non-NULL");
+    if (!aligned16(V) || !aligned4(W) || !aligned4(scores) || (A && !aligned4(A)))
+        return fail(DMA_ERR_INVALID_ARG, "V must be 16-byte aligned; W, A, scores 4-byte aligned");
+    if (key_begin < 0 || key_end < key_begin || key_end > S)
+        return fail(DMA_ERR_INVALID_ARG, "key range [%d, %d) outside [0, %d]", key_begin, key_end, S);
+    cudaError_t e = launch_score(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, scores,
+                                 reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
+    return ok();
+}
+
+dma_status_t dma_kept_layout(int B, int Hkv, int S, int w, int window, int block, dma_sel_mode_t mode,
+                             dma_kept_t* kept, size_t* select_ws_bytes)
+{
+    if (!kept || !select_ws_bytes) return fail(DMA_ERR_INVALID_ARG, "kept and select_ws_bytes must be non-NULL");
+    if (B < 1 || Hkv < 1 || S < 1) return fail(DMA_ERR_INVALID_ARG, "B=%d Hkv=%d S=%d must be >= 1", B, Hkv, S);
+    if (w < 0 || window < 0) return fail(DMA_ERR_INVALID_ARG, "w=%d and window=%d must be >= 0", w, window);
+    if (block != 1 && block != 64) return fail(DMA_ERR_UNSUPPORTED, "block=%d (supported: 1, 64)", block);
+    if (mode != DMA_SEL_ROWWISE && mode != DMA_SEL_GLOBAL) return fail(DMA_ERR_INVALID_ARG, "mode=%d", (int)mode);
+    if (S > (1 << 28) || (int64_t)B * Hkv * S > ((int64_t)1 << 34))
+        return fail(DMA_ERR_UNSUPPORTED, "selection over S=%d keys x %d segments is too large", S, B * Hkv);
+    dma_kept_t k = *kept;
+    k.B = B;
+    k.Hkv = Hkv;
+    k.S = S;
+    k.w = w;
+    k.window = window;
+    k.block = block;
+    k.mode = (int32_t)mode;
+    k.q_tile = kQTile;
+    k.n_qt = (S + kQTile - 1) / kQTile;
+    k.cap = S;
+    int64_t budget = kept_top_budget(w, S, block);
+    k.top_cap = (int32_t)(budget > 0 ? budget : 1);
+    int64_t stride = (int64_t)w + 3 * kQTile;
+    int64_t s4 = ((int64_t)S + 3) / 4 * 4;
+    if (stride > s4) stride = s4;
+    k.tile_stride = (int32_t)((stride + 3) / 4 * 4);
+    k.bitmap_words = ((S + kBitmapBlock - 1) / kBitmapBlock + 31) / 32;
+    *kept = k;
+    *select_ws_bytes = make_select_plan(B, Hkv, S, w, block).bytes;
+    return ok();
+}
+
+dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, int window, int block,
+                             dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len, dma_kept_t* kept, void* ws,
+                             size_t ws_bytes, dma_stream_t stream)
+{
+    if (!scores) return fail(DMA_ERR_INVALID_ARG, "scores is NULL");
+    if (!aligned4(scores)) return fail(DMA_ERR_INVALID_ARG, "scores must be 4-byte aligned");
+    dma_status_t s = check_kept_geometry(kept, B, Hkv, S);
+    if (s != DMA_OK) return s;
+    if (kept->w != w || kept->window != window || kept->block != block || kept->mode != (int32_t)mode)
+        return fail(DMA_ERR_INVALID_ARG, "kept layout (w=%d window=%d block=%d mode=%d) does not match the call",
+                    kept->w, kept->window, kept->block, kept->mode);
+    int* status = nullptr;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (op == DMA_SEL_UPDATE) {
+        if (block != 1) return fail(DMA_ERR_UNSUPPORTED, "UPDATE supports token units (block = 1) only");
+        if (!kept->top_idx || !kept->top_count) return fail(DMA_ERR_INVALID_ARG, "UPDATE needs top_idx and top_count");
+        if ((int64_t)kept->top_cap * 4 > 200 * 1024)
+            return fail(DMA_ERR_UNSUPPORTED, "UPDATE supports budgets up to 51200 keys");
+        if (seq_len && !aligned4(seq_len)) return fail(DMA_ERR_INVALID_ARG, "seq_len must be 4-byte aligned");
+        if ((s = status_ptr(&status)) != DMA_OK) return s;
+        cudaError_t e = launch_select_update(scores, kept, seq_len, status, st);
+        if (e != cudaSuccess) return cuda_fail(e, "select update launch");
+        return ok();
+    }
+    if (op != DMA_SEL_FULL) return fail(DMA_ERR_INVALID_ARG, "op=%d", (int)op);
+    if (seq_len) return fail(DMA_ERR_UNSUPPORTED, "FULL selection takes seq_len = NULL (all sequences of length S)");
+    if (!kept->expiry || !kept->idx || !kept->count)
+        return fail(DMA_ERR_INVALID_ARG, "FULL needs expiry, idx and count");
+    if ((kept->top_idx == nullptr) != (kept->top_count == nullptr))
+        return fail(DMA_ERR_INVALID_ARG, "top_idx and top_count must both be set or both be NULL");
+    if ((kept->tile_idx == nullptr) != (kept->tile_cnt == nullptr))
+        return fail(DMA_ERR_INVALID_ARG, "tile_idx and tile_cnt must both be set or both be NULL");
+    if (kept->bitmap && !kept->tile_idx) return fail(DMA_ERR_INVALID_ARG, "bitmap needs tile_idx/tile_cnt");
+    SelectPlan plan = make_select_plan(B, Hkv, S, w, block);
+    if (!ws || ws_bytes < plan.bytes)
+        return fail(DMA_ERR_WORKSPACE, "select workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
+                    plan.bytes);
+    if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if ((s = status_ptr(&status)) != DMA_OK) return s;
+    cudaError_t e = launch_select_full(scores, plan, kept, ws, status, st);
+    if (e != cudaSuccess) return cuda_fail(e, "select launch");
+    return ok();
+}
+
+dma_status_t dma_sparse_attn_prefill(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B, int S, int H,
+                                     int Hkv, int D, const float* scores, const dma_kept_t* kept, float scale,
+                                     void* O, float* lse, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (H < 1 || H % Hkv != 0) return fail(DMA_ERR_INVALID_ARG, "H=%d must be a positive multiple of Hkv=%d", H, Hkv);
+    if (!Q || !K || !V || !O || !scores) return fail(DMA_ERR_INVALID_ARG, "Q, K, V, O and scores must be non-NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned4(scores) || (lse && !aligned4(lse)))
+        return fail(DMA_ERR_INVALID_ARG, "Q, K, V, O must be 16-byte aligned; scores, lse 4-byte aligned");
+    if ((s = check_kept_geometry(kept, B, Hkv, S)) != DMA_OK) return s;
+    if (!kept->expiry || !kept->tile_cnt || !kept->tile_idx)
+        return fail(DMA_ERR_INVALID_ARG, "prefill needs kept->expiry, tile_cnt and tile_idx");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prefill_simt(Q, K, V, dt, B, S, H, Hkv, D, scores, kept, scale, O, lse, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return ok();
+}
+
+dma_status_t dma_decode_workspace_size(int B, int H, int Hkv, int D, int top_cap, int window, size_t* ws_bytes)
+{
+    if (!ws_bytes) return fail(DMA_ERR_INVALID_ARG, "ws_bytes is NULL");
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || top_cap < 0 || window < 0)
+        return fail(DMA_ERR_INVALID_ARG, "bad sizes B=%d H=%d Hkv=%d top_cap=%d window=%d", B, H, Hkv, top_cap, window);
+    if (D != 64 && D != 128) return fail(DMA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+    *ws_bytes = decode_ws_bytes(B, H, Hkv, D, top_cap, window);
+    return ok();
+}
+
+dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
+                                    const int32_t* cache_len, int H, int Hkv, int D, const float* scores,
+                                    const dma_kept_t* kept, float scale, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, Lmax, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (H < 1 || H % Hkv != 0) return fail(DMA_ERR_INVALID_ARG, "H=%d must be a positive multiple of Hkv=%d", H, Hkv);
+    if (H / Hkv > 16) return fail(DMA_ERR_UNSUPPORTED, "decode supports up to 16 query heads per KV head");
+    if (!q || !Kc || !Vc || !o || !scores) return fail(DMA_ERR_INVALID_ARG, "q, Kc, Vc, o and scores must be non-NULL");
+    if (!aligned16(q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(o) || !aligned4(scores) ||
+        (lse && !aligned4(lse)) || (cache_len && !aligned4(cache_len)))
+        return fail(DMA_ERR_INVALID_ARG, "q, Kc, Vc, o must be 16-byte aligned; scores, lse, cache_len 4-byte aligned");
+    if ((s = check_kept_geometry(kept, B, Hkv, Lmax)) != DMA_OK) return s;
+    if (!kept->top_idx || !kept->top_count) return fail(DMA_ERR_INVALID_ARG, "decode needs kept->top_idx/top_count");
+    size_t need = decode_ws_bytes(B, H, Hkv, D, kept->top_cap, kept->window);
+    if (!ws || ws_bytes < need)
+        return fail(DMA_ERR_WORKSPACE, "decode workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
+    cudaError_t e = launch_decode(q, Kc, Vc, dt, B, Lmax, cache_len, H, Hkv, D, scores, kept, scale, o, lse, ws,
+                                  reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal declarations shared by the CUDA translation units of libdma.
+// Nothing here is part of the C ABI (see include/dma.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dma.h"
+
+namespace dma {
+
+constexpr int kQTile = DMA_Q_TILE;
+constexpr int kBitmapBlock = 64;  // keys per bit of the occupancy bitmap
+
+// ---- small device helpers -------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// First row at which key j may enter the top set.
+__host__ __device__ __forceinline__ int top_lo(int j, int block)
+{
+    return block <= 1 ? j : (j / block) * block + block - 1;
+}
+
+// Records a device-side condition (first one wins).
+__device__ __forceinline__ void set_status(int* status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---- selection workspace --------------------------------------------------
+
+struct SelectPlan {
+    // problem
+    int nseg;       // B * Hkv
+    int S;          // keys per segment
+    int n;          // ranked units per segment (S for tokens, S / block for blocks)
+    int k;          // budget in units (w or w / block)
+    int nchunk;     // radix-sort chunks per segment
+    int T;          // rank chunk length of the expiry walk
+    int nC;         // ceil(n / T)
+    int X;          // position block length of the 2-D count table
+    int nX;         // ceil(n / X)
+    // byte offsets into the workspace
+    size_t off_key[2], off_val[2], off_hist, off_rank, off_tab, off_f0, off_bval, off_bexp;
+    size_t bytes;
+};
+
+SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block);
+
+// ---- launchers (host) -----------------------------------------------------
+
+cudaError_t launch_score(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
+                         const float* W, const float* A, float* scores, cudaStream_t st);
+
+cudaError_t launch_select_full(const float* scores, const SelectPlan& plan, const dma_kept_t* kept, void* ws,
+                               int* status, cudaStream_t st);
+cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len, int* status,
+                                 cudaStream_t st);
+
+cudaError_t launch_prefill_simt(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B, int S, int H,
+                                int Hkv, int D, const float* scores, const dma_kept_t* kept, float scale, void* O,
+                                float* lse, cudaStream_t st);
+
+size_t decode_ws_bytes(int B, int H, int Hkv, int D, int top_cap, int window);
+cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
+                          const int32_t* cache_len, int H, int Hkv, int D, const float* scores,
+                          const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, cudaStream_t st);
+
+}  // namespace dma

@@ -1,0 +1,816 @@
+// Causal top-w selection (Dynamic Mask Attention summary, lsdiaocha.cn, §五:
+// combine the dynamic weights with the causal mask, keep the top-k historical
+// positions at every time step, set the rest to -inf; §九: the keep budget is
+// fixed in advance).
+//
+// Output representation: one interval per key.  Key j is in the top set of rows
+// lo_j <= i < expiry[j].  For the row-wise rule this is exact because the top set
+// of row i+1 is the top set of row i plus key i+1, minus at most one evicted key:
+// once a key leaves it never returns.
+//
+// How expiry is computed (per (batch, KV head) segment of n ranked units):
+//  1. Sort the units best-first by (fp32 score desc, position asc): a stable
+//     4-pass LSD radix sort on an order-preserving 32-bit key, over chunks of
+//     2048 units (histogram -> digit-major scan -> stable scatter).  This gives
+//     p[t] (position of rank t) and rank[x].
+//  2. The keys that beat unit u are exactly the ranks below rank[u].  u is in
+//     the top set of row i iff fewer than k of them sit at positions <= i, so
+//       expiry[u] = max(u, f(rank[u])),  f(t) = k-th smallest of {p[0..t-1]}
+//     (f = infinity while t < k).  f is non-increasing in t.
+//  3. f over a rank chunk [tc, tc+T) is a staircase walk: start from f(tc),
+//     insert p[t] one at a time; an insertion below the current f moves f down
+//     to the largest inserted position below it, found 128 positions per step
+//     with warp ballots on rank[].  f(tc) itself comes from a 2-D count table
+//     (ranks < tc per position block of X) and one ballot pass inside a block.
+//  Global mode is rank[u] < k.  Block units run the same steps on block maxima
+//  over complete blocks and expand the block interval to its keys.
+//
+// Then: the ever-kept key list (ascending), the last row's top set, per query
+// tile of 128 rows the gathered key list (keys outside the window band whose
+// interval meets the tile) and the 64-key block occupancy bitmap.
+#include <cstdio>
+
+#include "dma_internal.cuh"
+
+namespace dma {
+
+namespace {
+
+constexpr int kRadixChunk = 2048;   // units per radix-sort chunk
+constexpr int kRadixThreads = 256;  // 8 warps x 8 rounds x 32 lanes
+constexpr int kRadixBins = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int pow2_ceil(int x)
+{
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+// Order-preserving key: ascending key = best first.  -0 is +0; NaN is last.
+__device__ __forceinline__ uint32_t rank_key(float s)
+{
+    if (s != s) return 0xffffffffu;
+    if (s == 0.f) s = 0.f;
+    uint32_t u = __float_as_uint(s);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending in s
+    return ~u;                                       // descending in s
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ---------------------------------------------------------------- block max --
+
+__global__ void block_max_kernel(const float* __restrict__ scores, int S, int nb, int block, float* __restrict__ bval)
+{
+    const int seg = blockIdx.y;
+    const int bk = blockIdx.x * blockDim.x + threadIdx.x;
+    if (bk >= nb) return;
+    const float* s = scores + (int64_t)seg * S + (int64_t)bk * block;
+    // The max is taken in key order, so the result is that of the keys' ranking
+    // keys: NaN ranks lowest and is skipped by fmaxf.
+    float m = -INFINITY;
+    bool any = false;
+    for (int t = 0; t < block; ++t) {
+        float v = s[t];
+        if (v == v) {
+            m = any ? fmaxf(m, v) : v;
+            any = true;
+        }
+    }
+    bval[(int64_t)seg * nb + bk] = any ? m : __int_as_float(0x7fc00000);
+}
+
+// ---------------------------------------------------------------- radix sort --
+
+// Pass input: either the raw values (first pass: key computed, value = position)
+// or the previous pass's (key, value) buffers.
+struct RadixIn {
+    const float* values;  // first pass only
+    const uint32_t* key;
+    const int32_t* val;
+};
+
+__device__ __forceinline__ void radix_load(const RadixIn& in, int64_t seg_base, int e, int n, uint32_t& key,
+                                           int32_t& val, bool& valid)
+{
+    valid = e < n;
+    key = 0;
+    val = 0;
+    if (!valid) return;
+    if (in.values) {
+        key = rank_key(in.values[seg_base + e]);
+        val = e;
+    } else {
+        key = in.key[seg_base + e];
+        val = in.val[seg_base + e];
+    }
+}
+
+__global__ void __launch_bounds__(kRadixThreads) radix_hist_kernel(RadixIn in, int n, int nchunk, int shift,
+                                                                   uint32_t* __restrict__ hist)
+{
+    __shared__ uint32_t h[kRadixBins];
+    const int seg = blockIdx.y, chunk = blockIdx.x;
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const int64_t seg_base = (int64_t)seg * n;
+    for (int r = 0; r < kRadixChunk / kRadixThreads; ++r) {
+        int e = chunk * kRadixChunk + r * kRadixThreads + threadIdx.x;
+        uint32_t key;
+        int32_t val;
+        bool valid;
+        radix_load(in, seg_base, e, n, key, val, valid);
+        if (valid) atomicAdd(&h[(key >> shift) & 0xff], 1u);
+    }
+    __syncthreads();
+    hist[((int64_t)seg * kRadixBins + threadIdx.x) * nchunk + chunk] = h[threadIdx.x];
+}
+
+// Exclusive scan of a segment's [digit][chunk] counts, in place.
+__global__ void __launch_bounds__(1024) radix_scan_kernel(uint32_t* __restrict__ hist, int nchunk)
+{
+    __shared__ uint32_t warp_tot[32];
+    __shared__ uint32_t carry;
+    const int seg = blockIdx.x;
+    uint32_t* h = hist + (int64_t)seg * kRadixBins * nchunk;
+    const int total = kRadixBins * nchunk;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < total; base += 1024) {
+        int e = base + threadIdx.x;
+        uint32_t v = e < total ? h[e] : 0;
+        uint32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t t = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_tot[lane] = t;  // inclusive over warps
+        }
+        __syncthreads();
+        uint32_t before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - v;
+        if (e < total) h[e] = before;
+        __syncthreads();
+        if (threadIdx.x == 0) carry += warp_tot[31];
+        __syncthreads();
+    }
+}
+
+// Stable scatter of one chunk.  Warp w owns units [w*256, w*256+256) of the
+// chunk and walks them in 8 rounds of 32, so (warp, round, lane) is the units'
+// original order; __match_any_sync groups the lanes of one digit in a round.
+__global__ void __launch_bounds__(kRadixThreads) radix_scatter_kernel(RadixIn in, int n, int nchunk, int shift,
+                                                                      const uint32_t* __restrict__ offs,
+                                                                      uint32_t* __restrict__ key_out,
+                                                                      int32_t* __restrict__ val_out, int* status)
+{
+    constexpr int kWarps = kRadixThreads / 32;
+    constexpr int kRounds = kRadixChunk / kRadixThreads;
+    __shared__ uint32_t wc[kWarps][kRadixBins];
+    __shared__ uint32_t gbase[kRadixBins];
+    const int seg = blockIdx.y, chunk = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int t = threadIdx.x; t < kWarps * kRadixBins; t += kRadixThreads) (&wc[0][0])[t] = 0;
+    gbase[threadIdx.x] = offs[((int64_t)seg * kRadixBins + threadIdx.x) * nchunk + chunk];
+    __syncthreads();
+
+    const int64_t seg_base = (int64_t)seg * n;
+    const uint32_t lt = lanemask_lt();
+    uint32_t key[kRounds];
+    int32_t val[kRounds];
+    uint32_t loc[kRounds];
+    int dig[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        int e = chunk * kRadixChunk + warp * (kRounds * 32) + r * 32 + lane;
+        bool valid;
+        radix_load(in, seg_base, e, n, key[r], val[r], valid);
+        int d = valid ? (int)((key[r] >> shift) & 0xff) : kRadixBins;
+        dig[r] = d;
+        uint32_t peers = __match_any_sync(0xffffffffu, d);
+        uint32_t rk = __popc(peers & lt);
+        loc[r] = valid ? wc[warp][d] + rk : 0;
+        __syncwarp();
+        if (valid && rk == 0) wc[warp][d] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    {
+        uint32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            uint32_t t = wc[w][threadIdx.x];
+            wc[w][threadIdx.x] = run;
+            run += t;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        int d = dig[r];
+        if (d < kRadixBins) {
+            uint32_t dl = gbase[d] + wc[warp][d] + loc[r];
+            if (dl < (uint32_t)n) {
+                key_out[seg_base + dl] = key[r];
+                val_out[seg_base + dl] = val[r];
+            } else {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+            }
+        }
+    }
+}
+
+__global__ void rank_kernel(const int32_t* __restrict__ p, int n, int32_t* __restrict__ rank, int* status)
+{
+    const int seg = blockIdx.y;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= n) return;
+    const int x = p[(int64_t)seg * n + t];
+    if (x >= 0 && x < n)
+        rank[(int64_t)seg * n + x] = t;
+    else
+        set_status(status, DMA_ERR_DEVICE_CHECK);
+}
+
+// ------------------------------------------------------------ expiry (global) --
+
+__global__ void global_expiry_kernel(const int32_t* __restrict__ rank, int n, int k, int32_t* __restrict__ E)
+{
+    const int seg = blockIdx.y;
+    const int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u < n) E[(int64_t)seg * n + u] = rank[(int64_t)seg * n + u] < k ? n : u;
+}
+
+// ---------------------------------------------------------- expiry (row-wise) --
+
+// tab[seg][c][xb] = number of ranks in chunk c whose position lies in block xb.
+__global__ void count_table_kernel(const int32_t* __restrict__ p, int n, int T, int nC, int X, int nX,
+                                   int32_t* __restrict__ tab)
+{
+    extern __shared__ int32_t cnt[];
+    const int seg = blockIdx.y, c = blockIdx.x;
+    for (int t = threadIdx.x; t < nX; t += blockDim.x) cnt[t] = 0;
+    __syncthreads();
+    const int t_end = min(n, (c + 1) * T);
+    for (int t = c * T + threadIdx.x; t < t_end; t += blockDim.x) {
+        const int x = p[(int64_t)seg * n + t];
+        if (x >= 0 && x < n) atomicAdd(&cnt[x / X], 1);
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < nX; t += blockDim.x) tab[((int64_t)seg * nC + c) * nX + t] = cnt[t];
+}
+
+// In place: tab[seg][c][xb] <- number of ranks < c*T in position block xb.
+__global__ void count_prefix_kernel(int32_t* __restrict__ tab, int nC, int nX)
+{
+    const int seg = blockIdx.x;
+    for (int xb = threadIdx.x; xb < nX; xb += blockDim.x) {
+        int32_t run = 0;
+        for (int c = 0; c < nC; ++c) {
+            int64_t o = ((int64_t)seg * nC + c) * nX + xb;
+            int32_t v = tab[o];
+            tab[o] = run;
+            run += v;
+        }
+    }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, <= 1024).
+__device__ int block_exclusive_scan(int v, int* warp_buf, int* total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_buf[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? warp_buf[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        warp_buf[lane] = t;
+    }
+    __syncthreads();
+    int before = (warp > 0 ? warp_buf[warp - 1] : 0) + x - v;
+    *total = warp_buf[nw - 1];
+    __syncthreads();
+    return before;
+}
+
+// f0[seg][c] = f(t_start) with t_start = max(c*T, k): the k-th smallest position
+// among ranks < t_start.  Only chunks that contain a rank >= k need it.
+constexpr int kBoundaryThreads = 256;
+__global__ void __launch_bounds__(kBoundaryThreads) boundary_kernel(const int32_t* __restrict__ p,
+                                                                   const int32_t* __restrict__ rank,
+                                                                   const int32_t* __restrict__ tab, int n, int k,
+                                                                   int T, int nC, int X, int nX,
+                                                                   int32_t* __restrict__ f0, int* status)
+{
+    extern __shared__ int32_t cnt[];  // [nX]
+    __shared__ int warp_buf[32];
+    __shared__ int sel_block, sel_need;
+    const int seg = blockIdx.y, c = blockIdx.x;
+    const int t_begin = c * T, t_end = min(n, t_begin + T);
+    const int t_start = max(t_begin, k);
+    if (t_start >= t_end) return;
+    if (k == 0) {
+        if (threadIdx.x == 0) f0[(int64_t)seg * nC + c] = -1;
+        return;
+    }
+    const int32_t* ps = p + (int64_t)seg * n;
+    const int32_t* rs = rank + (int64_t)seg * n;
+    for (int xb = threadIdx.x; xb < nX; xb += blockDim.x) cnt[xb] = tab[((int64_t)seg * nC + c) * nX + xb];
+    __syncthreads();
+    for (int t = t_begin + threadIdx.x; t < t_start; t += blockDim.x) {
+        const int x = ps[t];
+        if (x >= 0 && x < n) atomicAdd(&cnt[x / X], 1);
+    }
+    __syncthreads();
+    // find the position block holding the k-th smallest inserted position
+    if (threadIdx.x == 0) {
+        int run = 0, xb = 0;
+        for (; xb < nX; ++xb) {
+            if (run + cnt[xb] >= k) break;
+            run += cnt[xb];
+        }
+        sel_block = xb;
+        sel_need = k - run;  // 1-based order inside the block
+        // written first so that the walk never starts from an unset value
+        f0[(int64_t)seg * nC + c] = -1;
+        if (xb >= nX) set_status(status, DMA_ERR_DEVICE_CHECK);
+    }
+    __syncthreads();
+    const int xb = sel_block, need = sel_need;
+    if (xb >= nX) return;
+    // positions of the block, in ascending order, flagged if inserted (rank < t_start)
+    const int per = (X + blockDim.x - 1) / blockDim.x;
+    const int x_lo = xb * X + threadIdx.x * per;
+    int mine = 0;
+    for (int q = 0; q < per; ++q) {
+        int x = x_lo + q;
+        if (x < min(n, (xb + 1) * X) && rs[x] < t_start) ++mine;
+    }
+    int total;
+    int before = block_exclusive_scan(mine, warp_buf, &total);
+    if (need > before && need <= before + mine) {
+        int seen = before;
+        for (int q = 0; q < per; ++q) {
+            int x = x_lo + q;
+            if (x < min(n, (xb + 1) * X) && rs[x] < t_start) {
+                if (++seen == need) {
+                    f0[(int64_t)seg * nC + c] = x;
+                    break;
+                }
+            }
+        }
+    }
+}
+
+// One warp per (segment, rank chunk): E[p[t]] = max(p[t], f(t)).
+constexpr int kWalkWarps = 4;
+__global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const int32_t* __restrict__ p,
+                                                               const int32_t* __restrict__ rank,
+                                                               const int32_t* __restrict__ f0, int nseg, int n, int k,
+                                                               int T, int nC, int32_t* __restrict__ E, int* status)
+{
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kWalkWarps + (threadIdx.x >> 5);
+    if (gw >= nseg * nC) return;
+    const int seg = gw / nC, c = gw % nC;
+    const int32_t* ps = p + (int64_t)seg * n;
+    const int32_t* rs = rank + (int64_t)seg * n;
+    int32_t* Es = E + (int64_t)seg * n;
+    const int t_begin = c * T, t_end = min(n, t_begin + T);
+    const int t_start = min(t_end, max(t_begin, k));
+    // ranks below k: fewer than k keys beat them, they are never evicted
+    for (int t = t_begin + lane; t < t_start; t += 32) {
+        const int x = ps[t];
+        if (x >= 0 && x < n) Es[x] = n;
+    }
+    if (t_start >= t_end) return;
+    int x = f0[(int64_t)seg * nC + c];
+    if (x < -1 || x >= n) {
+        if (lane == 0) set_status(status, DMA_ERR_DEVICE_CHECK);
+        return;
+    }
+    for (int t0 = t_start; t0 < t_end; t0 += 32) {
+        const int my_t = t0 + lane;
+        int my_p = my_t < t_end ? ps[my_t] : 0;
+        if (my_p < 0 || my_p >= n) {
+            set_status(status, DMA_ERR_DEVICE_CHECK);
+            my_p = 0;
+        }
+        int my_x = 0;
+        const int steps = min(32, t_end - t0);
+        for (int q = 0; q < steps; ++q) {
+            const int pt = __shfl_sync(0xffffffffu, my_p, q);
+            if (lane == q) my_x = x;
+            if (pt < x) {
+                // f moves to the largest inserted position below x (p[t] itself qualifies)
+                const int t = t0 + q;
+                int base = x - 1;
+                for (;;) {
+                    int found = -1;
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        int pos = base - s * 32 - lane;
+                        bool flag = pos >= 0 && rs[pos] <= t;
+                        uint32_t m = __ballot_sync(0xffffffffu, flag);
+                        if (found < 0 && m) found = base - s * 32 - (__ffs(m) - 1);
+                    }
+                    if (found >= 0) {
+                        x = found;
+                        break;
+                    }
+                    base -= 128;
+                    if (base < 0) {  // cannot happen for a valid permutation: p[t] itself qualifies
+                        if (lane == 0) set_status(status, DMA_ERR_DEVICE_CHECK);
+                        x = -1;
+                        break;
+                    }
+                }
+            }
+        }
+        if (my_t < t_end) Es[my_p] = max(my_p, my_x);
+    }
+}
+
+// ------------------------------------------------------- block units -> keys --
+
+__global__ void expand_block_kernel(const int32_t* __restrict__ bexp, int S, int nb, int block,
+                                    int32_t* __restrict__ expiry)
+{
+    const int seg = blockIdx.y;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= S) return;
+    const int bk = j / block;
+    const int lo = bk * block + block - 1;
+    int e;
+    if (bk >= nb) {
+        e = min(lo, S);
+    } else {
+        const int E = bexp[(int64_t)seg * nb + bk];
+        if (E >= nb) {
+            e = S;
+        } else {
+            const int hi = E * block + block - 1;
+            e = hi > lo ? hi : lo;
+        }
+    }
+    expiry[(int64_t)seg * S + j] = e;
+}
+
+// ------------------------------------------------------------ compaction ------
+
+constexpr int kCompactThreads = 1024;
+// Per segment, in key order: idx <- keys ever in the top set; top <- keys in the
+// top set of the last row.
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const int32_t* __restrict__ expiry, int S,
+                                                                  int block, int32_t* __restrict__ idx,
+                                                                  int32_t* __restrict__ count,
+                                                                  int32_t* __restrict__ top_idx,
+                                                                  int32_t* __restrict__ top_count, int top_cap,
+                                                                  int* status)
+{
+    __shared__ int warp_buf[32];
+    const int seg = blockIdx.x;
+    const int32_t* ex = expiry + (int64_t)seg * S;
+    int run_all = 0, run_top = 0;
+    for (int base = 0; base < S; base += kCompactThreads) {
+        const int j = base + threadIdx.x;
+        int lo = top_lo(j, block);
+        int e = j < S ? ex[j] : 0;
+        int ever = (j < S && lo < e) ? 1 : 0;
+        int last = (ever && e >= S) ? 1 : 0;
+        int tot_all, tot_top;
+        int b_all = block_exclusive_scan(ever, warp_buf, &tot_all);
+        int b_top = block_exclusive_scan(last, warp_buf, &tot_top);
+        if (ever) idx[(int64_t)seg * S + run_all + b_all] = j;
+        if (last && top_idx) {
+            int o = run_top + b_top;
+            if (o < top_cap)
+                top_idx[(int64_t)seg * top_cap + o] = j;
+            else
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+        }
+        run_all += tot_all;
+        run_top += tot_top;
+    }
+    if (threadIdx.x == 0) {
+        count[seg] = run_all;
+        if (top_count) top_count[seg] = min(run_top, top_cap);
+    }
+}
+
+// ----------------------------------------------------------- per-tile lists ---
+
+constexpr int kTileThreads = 256;
+// For query tile [q0, q1]: keys j <= lim (lim = q0 - window, or q1 without a
+// window) with lo_j <= q1 and expiry_j > q0, ascending; plus the bitmap of
+// 64-key blocks holding a kept key (gathered keys and the window band).
+__global__ void __launch_bounds__(kTileThreads) tile_list_kernel(const int32_t* __restrict__ expiry,
+                                                                 const int32_t* __restrict__ idx,
+                                                                 const int32_t* __restrict__ count, int S, int block,
+                                                                 int window, int n_qt, int tile_stride,
+                                                                 int bitmap_words, int32_t* __restrict__ tile_cnt,
+                                                                 int32_t* __restrict__ tile_idx,
+                                                                 uint32_t* __restrict__ bitmap, int* status)
+{
+    extern __shared__ uint32_t bm[];  // [bitmap_words]
+    __shared__ int warp_buf[32];
+    __shared__ int stop;
+    const int seg = blockIdx.y, tile = blockIdx.x;
+    const int q0 = tile * kQTile, q1 = min(S, q0 + kQTile) - 1;
+    const int lim = window > 0 ? q0 - window : q1;
+    const int32_t* ex = expiry + (int64_t)seg * S;
+    const int32_t* li = idx + (int64_t)seg * S;
+    const int n = count[seg];
+    int32_t* out = tile_idx + ((int64_t)seg * n_qt + tile) * tile_stride;
+    if (bitmap)
+        for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bm[t] = 0;
+    if (threadIdx.x == 0) stop = 0;
+    __syncthreads();
+    int run = 0;
+    for (int base = 0; base < n; base += kTileThreads) {
+        const int u = base + threadIdx.x;
+        int j = u < n ? li[u] : INT32_MAX;
+        int act = 0;
+        if (j < 0 || (j >= S && j != INT32_MAX)) {
+            set_status(status, DMA_ERR_DEVICE_CHECK);
+            j = INT32_MAX;
+        }
+        if (j <= lim) {
+            int e = ex[j];
+            act = (top_lo(j, block) <= q1 && e > q0) ? 1 : 0;
+        }
+        if (u < n && j > lim) stop = 1;  // the list is ascending: nothing later qualifies
+        int tot;
+        int before = block_exclusive_scan(act, warp_buf, &tot);
+        if (act) {
+            int o = run + before;
+            if (o < tile_stride)
+                out[o] = j;
+            else
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+            if (bitmap) atomicOr(&bm[j / (kBitmapBlock * 32)], 1u << ((j / kBitmapBlock) & 31));
+        }
+        run += tot;
+        __syncthreads();
+        if (stop) break;
+    }
+    if (threadIdx.x == 0) tile_cnt[(int64_t)seg * n_qt + tile] = min(run, tile_stride);
+    if (bitmap) {
+        if (window > 0) {
+            const int band_lo = max(0, q0 - window + 1);
+            for (int b64 = band_lo / kBitmapBlock + threadIdx.x; b64 <= q1 / kBitmapBlock; b64 += kTileThreads)
+                atomicOr(&bm[b64 / 32], 1u << (b64 & 31));
+        }
+        __syncthreads();
+        uint32_t* bo = bitmap + ((int64_t)seg * n_qt + tile) * bitmap_words;
+        for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bo[t] = bm[t];
+    }
+}
+
+// ---------------------------------------------------------------- update ----
+
+constexpr int kUpdateThreads = 1024;
+// top set of row t = top-w(top set of row t-1 + key t), t = seq_len[b] - 1.
+__global__ void __launch_bounds__(kUpdateThreads) update_kernel(const float* __restrict__ scores, int Hkv, int S,
+                                                                const int32_t* __restrict__ seq_len,
+                                                                int32_t* __restrict__ top_idx,
+                                                                int32_t* __restrict__ top_count, int top_cap,
+                                                                int budget, int* status)
+{
+    extern __shared__ int32_t buf[];  // [budget]
+    __shared__ uint32_t red_key[32];
+    __shared__ int red_pos[32];
+    __shared__ int worst_pos;
+    const int seg = blockIdx.x;
+    const int b = seg / Hkv;
+    const int t = seq_len ? seq_len[b] - 1 : S - 1;
+    const float* sc = scores + (int64_t)seg * S;
+    int32_t* ti = top_idx + (int64_t)seg * top_cap;
+    const int cnt = top_count[seg];
+    if (t < 0 || t >= S || cnt < 0 || cnt > budget || (cnt > 0 && ti[cnt - 1] >= t)) {
+        if (threadIdx.x == 0) set_status(status, DMA_ERR_DEVICE_CHECK);
+        return;
+    }
+    if (budget == 0) return;
+    if (cnt < budget) {
+        if (threadIdx.x == 0) {
+            ti[cnt] = t;
+            top_count[seg] = cnt + 1;
+        }
+        return;
+    }
+    // worst member: largest ranking key, ties to the larger index (= later position in the list)
+    uint32_t wk = 0;
+    int wp = -1;
+    for (int u = threadIdx.x; u < cnt; u += kUpdateThreads) {
+        int j = ti[u];
+        buf[u] = j;
+        if (j < 0 || j >= S) {
+            set_status(status, DMA_ERR_DEVICE_CHECK);
+            j = 0;
+        }
+        uint32_t kk = rank_key(sc[j]);
+        if (wp < 0 || kk > wk || (kk == wk && u > wp)) {
+            wk = kk;
+            wp = u;
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        uint32_t ok = __shfl_xor_sync(0xffffffffu, wk, o);
+        int op = __shfl_xor_sync(0xffffffffu, wp, o);
+        if (op >= 0 && (wp < 0 || ok > wk || (ok == wk && op > wp))) {
+            wk = ok;
+            wp = op;
+        }
+    }
+    if (lane == 0) {
+        red_key[warp] = wk;
+        red_pos[warp] = wp;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t bk = 0;
+        int bp = -1;
+        for (int w = 0; w < kUpdateThreads / 32; ++w) {
+            int op = red_pos[w];
+            uint32_t ok = red_key[w];
+            if (op >= 0 && (bp < 0 || ok > bk || (ok == bk && op > bp))) {
+                bk = ok;
+                bp = op;
+            }
+        }
+        // the newest key has the largest index: it enters only with a strictly better score
+        worst_pos = rank_key(sc[t]) < bk ? bp : -1;
+    }
+    __syncthreads();
+    const int wpos = worst_pos;
+    if (wpos < 0) return;
+    for (int u = wpos + threadIdx.x; u < cnt - 1; u += kUpdateThreads) ti[u] = buf[u + 1];
+    if (threadIdx.x == 0) ti[cnt - 1] = t;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- host ----
+
+SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block)
+{
+    SelectPlan pl{};
+    pl.nseg = B * Hkv;
+    pl.S = S;
+    pl.n = block <= 1 ? S : S / block;
+    pl.k = block <= 1 ? w : w / block;
+    if (pl.k > pl.n) pl.k = pl.n;
+    const int n = pl.n > 0 ? pl.n : 1;
+    pl.nchunk = (n + kRadixChunk - 1) / kRadixChunk;
+    pl.T = pl.X = std::max(64, pow2_ceil((n + 127) / 128));
+    pl.nC = (n + pl.T - 1) / pl.T;
+    pl.nX = (n + pl.X - 1) / pl.X;
+    const size_t nu = (size_t)pl.nseg * n;
+    size_t o = 0;
+    for (int i = 0; i < 2; ++i) {
+        pl.off_key[i] = o;
+        o = align_up(o + nu * 4, 256);
+        pl.off_val[i] = o;
+        o = align_up(o + nu * 4, 256);
+    }
+    pl.off_hist = o;
+    o = align_up(o + (size_t)pl.nseg * kRadixBins * pl.nchunk * 4, 256);
+    pl.off_rank = o;
+    o = align_up(o + nu * 4, 256);
+    pl.off_tab = o;
+    o = align_up(o + (size_t)pl.nseg * pl.nC * pl.nX * 4, 256);
+    pl.off_f0 = o;
+    o = align_up(o + (size_t)pl.nseg * pl.nC * 4, 256);
+    pl.off_bval = o;
+    pl.off_bexp = o;
+    if (block > 1) {
+        o = align_up(o + nu * 4, 256);
+        pl.off_bexp = o;
+        o = align_up(o + nu * 4, 256);
+    }
+    pl.bytes = o;
+    return pl;
+}
+
+cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const dma_kept_t* kept, void* ws,
+                               int* status, cudaStream_t st)
+{
+    char* W = static_cast<char*>(ws);
+    const int nseg = pl.nseg, n = pl.n, S = pl.S, block = kept->block;
+    uint32_t* keyb[2] = {reinterpret_cast<uint32_t*>(W + pl.off_key[0]), reinterpret_cast<uint32_t*>(W + pl.off_key[1])};
+    int32_t* valb[2] = {reinterpret_cast<int32_t*>(W + pl.off_val[0]), reinterpret_cast<int32_t*>(W + pl.off_val[1])};
+    uint32_t* hist = reinterpret_cast<uint32_t*>(W + pl.off_hist);
+    int32_t* rank = reinterpret_cast<int32_t*>(W + pl.off_rank);
+    int32_t* tab = reinterpret_cast<int32_t*>(W + pl.off_tab);
+    int32_t* f0 = reinterpret_cast<int32_t*>(W + pl.off_f0);
+    float* bval = reinterpret_cast<float*>(W + pl.off_bval);
+    int32_t* bexp = reinterpret_cast<int32_t*>(W + pl.off_bexp);
+    cudaError_t e;
+
+    const float* unit_values = scores;
+    int32_t* E = kept->expiry;  // token units: the unit expiry is the key expiry
+    if (block > 1) {
+        unit_values = bval;
+        E = bexp;
+        if (n > 0) {
+            block_max_kernel<<<dim3((n + 127) / 128, nseg), 128, 0, st>>>(scores, S, n, block, bval);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    }
+    if (n > 0) {
+        // 1. sort units best-first
+        for (int pass = 0; pass < 4; ++pass) {
+            RadixIn in{};
+            if (pass == 0) {
+                in.values = unit_values;
+            } else {
+                in.key = keyb[(pass - 1) & 1];
+                in.val = valb[(pass - 1) & 1];
+            }
+            const int shift = 8 * pass;
+            dim3 grid(pl.nchunk, nseg);
+            radix_hist_kernel<<<grid, kRadixThreads, 0, st>>>(in, n, pl.nchunk, shift, hist);
+            radix_scan_kernel<<<nseg, 1024, 0, st>>>(hist, pl.nchunk);
+            radix_scatter_kernel<<<grid, kRadixThreads, 0, st>>>(in, n, pl.nchunk, shift, hist, keyb[pass & 1],
+                                                                 valb[pass & 1], status);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        const int32_t* p = valb[1];
+        rank_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(p, n, rank, status);
+        // 2-3. unit expiry
+        if (kept->mode == DMA_SEL_GLOBAL) {
+            global_expiry_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(rank, n, pl.k, E);
+        } else {
+            count_table_kernel<<<dim3(pl.nC, nseg), 256, pl.nX * 4, st>>>(p, n, pl.T, pl.nC, pl.X, pl.nX, tab);
+            count_prefix_kernel<<<nseg, 128, 0, st>>>(tab, pl.nC, pl.nX);
+            boundary_kernel<<<dim3(pl.nC, nseg), kBoundaryThreads, pl.nX * 4, st>>>(p, rank, tab, n, pl.k, pl.T,
+                                                                                    pl.nC, pl.X, pl.nX, f0, status);
+            const int walkers = nseg * pl.nC;
+            walk_kernel<<<(walkers + kWalkWarps - 1) / kWalkWarps, kWalkWarps * 32, 0, st>>>(p, rank, f0, nseg, n,
+                                                                                            pl.k, pl.T, pl.nC, E, status);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (block > 1) {
+        expand_block_kernel<<<dim3((S + 255) / 256, nseg), 256, 0, st>>>(bexp, S, n, block, kept->expiry);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 4. lists
+    compact_kernel<<<nseg, kCompactThreads, 0, st>>>(kept->expiry, S, block, kept->idx, kept->count, kept->top_idx,
+                                                     kept->top_count, kept->top_cap, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (kept->tile_idx) {
+        tile_list_kernel<<<dim3(kept->n_qt, nseg), kTileThreads, kept->bitmap ? kept->bitmap_words * 4 : 0, st>>>(
+            kept->expiry, kept->idx, kept->count, S, block, kept->window, kept->n_qt, kept->tile_stride,
+            kept->bitmap_words, kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len, int* status,
+                                 cudaStream_t st)
+{
+    const int nseg = kept->B * kept->Hkv;
+    const int budget = kept->w < kept->S ? kept->w : kept->S;
+    size_t smem = (size_t)(budget > 0 ? budget : 1) * 4;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    update_kernel<<<nseg, kUpdateThreads, smem, st>>>(scores, kept->Hkv, kept->S, seq_len, kept->top_idx,
+                                                     kept->top_count, kept->top_cap, budget, status);
+    return cudaGetLastError();
+}
+
+}  // namespace dma

@@ -104,27 +104,43 @@ def make_prefill(B: int, S: int, H: int, Hkv: int, D: int, dtype: torch.dtype, s
 
 
 def make_decode(B: int, L: int, H: int, Hkv: int, D: int, dtype: torch.dtype, seed: int, salient: bool = True,
-                n_queries: int = 1):
-    """Seeded decode inputs on the CPU: ``n_queries`` new query rows per sequence.
+                n_queries: int = 1, device="cpu", batches=None):
+    """Seeded decode inputs: ``n_queries`` new query rows per sequence.
 
-    Returns W [Hkv][D] fp32, q [n_queries][B][H][D] and the caches Kc, Vc
-    [B][L][Hkv][D] in ``dtype``.  Position ``L - n_queries + k`` of the cache
-    holds the key/value of the token that query ``k`` belongs to.
+    Returns W [Hkv][D] fp32, q [n_queries][B'][H][D] and the caches Kc, Vc
+    [B'][L][Hkv][D] in ``dtype``, on ``device``.  Position ``L - n_queries + k``
+    of the cache holds the key/value of the token that query ``k`` belongs to.
+
+    Each sequence b draws from its own generator (seed * 7919 + b + 1; order q,
+    K, V, salient mask), so ``batches`` -- a subset of range(B) -- regenerates
+    exactly those sequences (B' = len(batches)) without drawing the others.
+    The values depend on ``device`` (CPU and CUDA generators differ).
     """
     g = torch.Generator().manual_seed(seed)
     W = _randn(g, (Hkv, D)) * (1.0 / D) ** 0.5
-    q = _randn(g, (n_queries, B, H, D))
-    Kc = _randn(g, (B, L, Hkv, D))
-    Vc = _randn(g, (B, L, Hkv, D))
-    if salient:
-        _apply_salient(g, Kc, Vc)
-    return {"W": W.contiguous(), "A": None, "q": q.to(dtype).contiguous(), "Kc": Kc.to(dtype).contiguous(),
-            "Vc": Vc.to(dtype).contiguous()}
+    batches = list(range(B)) if batches is None else list(batches)
+    nb = len(batches)
+    q = torch.empty((n_queries, nb, H, D), dtype=dtype, device=device)
+    Kc = torch.empty((nb, L, Hkv, D), dtype=dtype, device=device)
+    Vc = torch.empty((nb, L, Hkv, D), dtype=dtype, device=device)
+    for r, b in enumerate(batches):
+        gb = torch.Generator(device=device).manual_seed(seed * 7919 + b + 1)
+        q[:, r] = torch.randn((n_queries, H, D), generator=gb, device=device).to(dtype)
+        k = torch.randn((L, Hkv, D), generator=gb, device=device)
+        v = torch.randn((L, Hkv, D), generator=gb, device=device)
+        if salient:
+            mask = torch.rand((L, Hkv), generator=gb, device=device) < 0.05
+            k[mask] *= 3.0
+            v[mask] *= 3.0
+        Kc[r] = k.to(dtype)
+        Vc[r] = v.to(dtype)
+    return {"W": W.contiguous().to(device), "A": None, "q": q, "Kc": Kc, "Vc": Vc}
 
 
-def make_workload(wl: Workload, n_queries: int = 1):
+def make_workload(wl: Workload, n_queries: int = 1, device="cpu", batches=None):
     if wl.decode:
-        return make_decode(wl.B, wl.S, wl.H, wl.Hkv, wl.D, wl.torch_dtype, wl.seed, wl.salient, n_queries)
+        return make_decode(wl.B, wl.S, wl.H, wl.Hkv, wl.D, wl.torch_dtype, wl.seed, wl.salient, n_queries,
+                           device=device, batches=batches)
     return make_prefill(wl.B, wl.S, wl.H, wl.Hkv, wl.D, wl.torch_dtype, wl.seed, wl.salient)
 
 

@@ -1,0 +1,206 @@
+/*
+ * dma.h -- C ABI of the B300 (sm_103a) dynamic-mask sparse attention library.
+ *
+ * The method (Dynamic Mask Attention summary, lsdiaocha.cn, §四 and §五): every
+ * key gets a content-derived importance score per KV head; at every time step
+ * each head keeps the top-w historical keys (causal mask first, then top-k, the
+ * rest set to -inf), optionally united with a local window; softmax attention
+ * runs over the kept keys only, with the score added to the logit as a bias.
+ * Skipped positions would have weight exactly 0, so skipping them computes the
+ * same result as the full masked attention.
+ *
+ * Four calls make the forward hot path:
+ *   dma_score_keys           s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>)
+ *   dma_select_topk          per-key top-set intervals + per-query-tile key lists
+ *   dma_sparse_attn_prefill  masked softmax attention over the kept keys
+ *   dma_sparse_attn_decode   the same for one new query row per sequence
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and frees every buffer; the library never
+ *     allocates device memory.  Pointers named "device" must be device memory
+ *     of the current CUDA device; nothing is read on the host except scalars.
+ *   - Layout: dense, row-major, innermost dimension last, as written beside
+ *     each argument.  Q [B][S][H][D]; K, V [B][S][Hkv][D]; query head hq uses
+ *     KV head hq / (H / Hkv).  Every tensor base must be 16-byte aligned.
+ *   - Supported shapes: D in {64, 128}; H % Hkv == 0; S >= 1; w >= 0;
+ *     window >= 0.  dtype DMA_F32 or DMA_BF16 (round-to-nearest-even output).
+ *   - Streams: every call only enqueues work on `stream` (NULL = the legacy
+ *     default stream) and never synchronises, except dma_get_device_status.
+ *   - Errors: argument errors return DMA_ERR_INVALID_ARG / DMA_ERR_UNSUPPORTED /
+ *     DMA_ERR_WORKSPACE before anything is launched; a failed launch returns
+ *     DMA_ERR_CUDA.  dma_last_error_message() gives a per-thread detail string.
+ *     Conditions found on the device (a bounded wait that ran out, an internal
+ *     capacity check) set a device status word read by dma_get_device_status.
+ *   - Outputs alias no input.
+ */
+#ifndef DMA_H_
+#define DMA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dma_stream_t; /* a cudaStream_t */
+
+typedef enum {
+    DMA_OK = 0,
+    DMA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned base, mismatched layout */
+    DMA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. D = 96) */
+    DMA_ERR_WORKSPACE = 3,    /* workspace pointer null or smaller than the size query says */
+    DMA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    DMA_ERR_TIMEOUT = 5,      /* device status: a bounded wait inside a kernel ran out */
+    DMA_ERR_DEVICE_CHECK = 6  /* device status: an internal capacity/bounds check failed */
+} dma_status_t;
+
+typedef enum { DMA_F32 = 0, DMA_BF16 = 1 } dma_dtype_t;
+
+/* Row-wise: row i keeps the min(w, i+1) best keys among 0..i (top-k at every
+ * time step, DMA summary §五).  Global: row i keeps the keys j <= i that are
+ * among the w best of all S keys.  Both coincide on the last row. */
+typedef enum { DMA_SEL_ROWWISE = 0, DMA_SEL_GLOBAL = 1 } dma_sel_mode_t;
+
+/* FULL recomputes everything from the score array.  UPDATE (decode) merges the
+ * newest key of each sequence into the top set of the previous row. */
+typedef enum { DMA_SEL_FULL = 0, DMA_SEL_UPDATE = 1 } dma_sel_op_t;
+
+/* Rows per query tile of the per-tile key lists. */
+#define DMA_Q_TILE 128
+
+/*
+ * The kept-key representation.  Geometry fields are filled by dma_kept_layout;
+ * the caller then allocates the arrays (device memory) and sets the pointers.
+ *
+ * Every key j has one top-set interval: j is in the top set of rows
+ * lo_j <= i < expiry[j], where lo_j = j for token units (block == 1) and the
+ * last key of j's block, (j / block) * block + block - 1, for block units.
+ * expiry[j] <= lo_j means the key never enters the top set (it is then
+ * min(lo_j, S)); expiry[j] == S means it is still kept at the last row.
+ * The kept set of row i is that top set united with {i-window+1 .. i}.
+ */
+typedef struct {
+    /* geometry (written by dma_kept_layout, checked by every consumer) */
+    int32_t B, Hkv, S, w, window, block, mode;
+    int32_t q_tile;       /* DMA_Q_TILE */
+    int32_t n_qt;         /* ceil(S / q_tile) query tiles */
+    int32_t cap;          /* entries of idx per (b, h) = S */
+    int32_t top_cap;      /* entries of top_idx per (b, h): the top-set size bound */
+    int32_t tile_stride;  /* entries of tile_idx per (b, h, tile) */
+    int32_t bitmap_words; /* 32-bit words of bitmap per (b, h, tile) = ceil(S / 64 / 32) */
+    /* caller-owned device arrays */
+    int32_t* expiry;      /* [B][Hkv][S]                       required (FULL) */
+    int32_t* idx;         /* [B][Hkv][cap]  keys ever kept by the top rule, ascending; required (FULL) */
+    int32_t* count;       /* [B][Hkv]       entries used in idx; required (FULL) */
+    int32_t* top_idx;     /* [B][Hkv][top_cap] top set of the last row, ascending; nullable (FULL),
+                                            required (UPDATE and decode) */
+    int32_t* top_count;   /* [B][Hkv]                           with top_idx */
+    int32_t* tile_cnt;    /* [B][Hkv][n_qt]                     required by prefill */
+    int32_t* tile_idx;    /* [B][Hkv][n_qt][tile_stride]: keys j <= q0 - window (all j <= q1 when
+                                            window == 0) whose top interval meets the tile's rows
+                                            [q0, q1], ascending; the window band (q0-window, q1]
+                                            is implicit */
+    uint32_t* bitmap;     /* [B][Hkv][n_qt][bitmap_words]: bit (tile, 64-key block) set iff some key
+                                            of the block is kept by some row of the tile; nullable */
+} dma_kept_t;
+
+/* ---------------------------------------------------------------- scoring --
+ * DMA summary §五, dynamic weight delta = exp(tau(v Delta) * A): with tau =
+ * softplus, Delta a per-KV-head vector W[h] and A a per-KV-head gate, the log
+ * weight s = A_h * softplus(v . W[h]) is the additive logit bias and the
+ * ranking key.
+ *   V       device [B][S][Hkv][D] (dtype dt)   value rows
+ *   W       device [Hkv][D] fp32               per-KV-head sampling weights
+ *   A       device [Hkv] fp32 or NULL (= 1)    per-KV-head gate
+ *   scores  device [B][Hkv][S] fp32            written for key_begin <= j < key_end only
+ * 0 <= key_begin <= key_end <= S.  key_begin == key_end is a no-op.
+ */
+dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
+                            int key_end, const float* W, const float* A, float* scores, dma_stream_t stream);
+
+/* -------------------------------------------------------------- selection --
+ * Fills the geometry of *kept for the given problem (pointers untouched) and
+ * the workspace size dma_select_topk needs.  block is 1 (token units) or 64
+ * (64-key blocks: block score = max of its keys' scores; row i ranks complete
+ * blocks only, keeps floor(w / 64) of them).
+ */
+dma_status_t dma_kept_layout(int B, int Hkv, int S, int w, int window, int block, dma_sel_mode_t mode,
+                             dma_kept_t* kept, size_t* select_ws_bytes);
+
+/* DMA summary §五: combine the scores with the causal mask, keep the top-w at
+ * every time step.  Ties go to the lower key index; scores are compared as
+ * fp32 (-0 equals +0; NaN ranks below every number).
+ *   scores   device [B][Hkv][S] fp32
+ *   kept     geometry from dma_kept_layout with the same (B, Hkv, S, w, window,
+ *            block, mode); arrays as documented in dma_kept_t
+ *   op       FULL: writes expiry, idx/count, and (when non-NULL) top_idx/top_count,
+ *            tile_cnt/tile_idx and bitmap.
+ *            UPDATE: token units only; the newest key of sequence b sits at
+ *            position seq_len[b] - 1 (seq_len NULL: S - 1); top_idx/top_count
+ *            must hold the top set of the previous row; it becomes top-w of
+ *            (previous set + newest key).  Nothing else is written.
+ *   seq_len  device [B] int32 or NULL.  FULL requires NULL (all sequences have
+ *            length S).
+ *   ws       device workspace of at least *select_ws_bytes (FULL); UPDATE needs none.
+ */
+dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, int window, int block,
+                             dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len, dma_kept_t* kept,
+                             void* ws, size_t ws_bytes, dma_stream_t stream);
+
+/* -------------------------------------------------------------- attention --
+ * DMA summary §四/§五: masked positions are skipped outright; the kept ones get
+ * x_ij = scale * <Q_i, K_j> + s_j, softmax over the kept set, O_i = sum p_ij V_j.
+ *   Q        device [B][S][H][D]      K, V  device [B][S][Hkv][D]   (dtype dt)
+ *   scores   device [B][Hkv][S] fp32  (the bias; the same array the selection used)
+ *   kept     after dma_select_topk(FULL) with tile_cnt/tile_idx set
+ *   scale    > 0, or <= 0 for 1/sqrt(D)
+ *   O        device [B][S][H][D] (dtype dt)
+ *   lse      device [B][H][S] fp32 or NULL: log-sum-exp of the kept logits
+ * A row with nothing kept gets O = 0 and lse = -inf.
+ */
+dma_status_t dma_sparse_attn_prefill(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B, int S,
+                                     int H, int Hkv, int D, const float* scores, const dma_kept_t* kept,
+                                     float scale, void* O, float* lse, dma_stream_t stream);
+
+/* Workspace bytes of dma_sparse_attn_decode. */
+dma_status_t dma_decode_workspace_size(int B, int H, int Hkv, int D, int top_cap, int window, size_t* ws_bytes);
+
+/* One new query row per sequence, at position L-1 of its cache of length
+ * L = cache_len[b]; same kept-set rule as the last prefill row (DMA summary
+ * §七: the same sparsity in training and inference; the full cache is kept and
+ * only the selection changes).
+ *   q          device [B][H][D]            Kc, Vc device [B][Lmax][Hkv][D]
+ *   cache_len  device [B] int32 or NULL (= Lmax); 1 <= L <= Lmax
+ *   scores     device [B][Hkv][Lmax] fp32
+ *   kept       top_idx/top_count = the top set of row L-1 (FULL at S = L, or UPDATE)
+ *   o          device [B][H][D] (dtype dt)    lse device [B][H] fp32 or NULL
+ *   ws         device workspace of dma_decode_workspace_size bytes
+ */
+dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
+                                    const int32_t* cache_len, int H, int Hkv, int D, const float* scores,
+                                    const dma_kept_t* kept, float scale, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, dma_stream_t stream);
+
+/* ------------------------------------------------------------------ misc -- */
+
+/* Synchronises `stream`, returns the device status word (a dma_status_t value,
+ * DMA_OK if nothing was recorded) in *device_status and clears it. */
+dma_status_t dma_get_device_status(dma_stream_t stream, int* device_status);
+
+const char* dma_status_string(dma_status_t s);
+
+/* Detail of the last failing call on this host thread ("" if none). */
+const char* dma_last_error_message(void);
+
+/* Selects the prefill kernel: 0 = automatic (tensor-core kernel for bf16 when
+ * available), 1 = SIMT kernel always.  Process-wide; returns the old value. */
+int dma_set_prefill_kernel(int which);
+
+int dma_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMA_H_ */

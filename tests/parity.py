@@ -1,0 +1,141 @@
+"""Comparison rules between the CUDA path and the fp64 oracle (test infrastructure).
+
+* Kept sets match exactly, except keys whose fp32 ranking value lies within
+  ``TIE_TOL`` of that row's cutoff (the smallest ranking value in the oracle's
+  top set; for global mode the global cutoff).  fp32 scores computed in a
+  different summation order can swap such near-ties, which is the only freedom
+  the comparison grants.  Rows touched by a swap are left out of the output
+  comparison (the oracle is never fed a GPU-derived set).
+* Outputs match within a max-abs error of 1e-4 (fp32 inputs) or 2e-2 (bf16),
+  for O and for lse.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+TIE_TOL = 1e-5
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+SCORE_ATOL = 5e-5
+SCORE_RTOL = 1e-5
+
+
+def top_lo(S: int, block: int) -> np.ndarray:
+    j = np.arange(S)
+    return j if block <= 1 else (j // block) * block + block - 1
+
+
+def unit_values(scores32: np.ndarray, block: int) -> np.ndarray:
+    """Ranking value of each key's unit: its fp32 score, or its block's max."""
+    if block <= 1:
+        return scores32
+    S = scores32.shape[-1]
+    nb = S // block
+    out = np.full(S, -np.inf, dtype=np.float64)
+    if nb:
+        bm = scores32[:nb * block].reshape(nb, block).max(axis=1)
+        out[:nb * block] = np.repeat(bm, block)
+    return out
+
+
+def check_scores(gpu: torch.Tensor, ref: torch.Tensor, key_begin: int = 0, key_end=None):
+    g = gpu.double().cpu()[..., key_begin:key_end]
+    r = ref[..., key_begin:key_end]
+    err = (g - r).abs()
+    bound = SCORE_ATOL + SCORE_RTOL * r.abs()
+    assert bool((err <= bound).all()), "score error %.3g > bound" % float((err - bound).max())
+
+
+def check_expiry(gpu_ex: torch.Tensor, or_ex: torch.Tensor, or_scores: torch.Tensor, w: int, block: int,
+                 mode: int, max_rows: int = 5000):
+    """Compares per-key top-set intervals.  Returns {(b, h): set of rows whose
+    kept set differs by a near-tie}; raises on any other difference."""
+    g = gpu_ex.cpu().numpy()
+    o = or_ex.cpu().numpy()
+    s32 = or_scores.cpu().numpy().astype(np.float32).astype(np.float64)
+    B, Hkv, S = o.shape
+    lo = top_lo(S, block)
+    affected = {}
+    checked = 0
+    for b in range(B):
+        for h in range(Hkv):
+            bad = np.nonzero(g[b, h] != o[b, h])[0]
+            if len(bad) == 0:
+                continue
+            val = unit_values(s32[b, h], block)
+            if mode == 1:
+                win = (o[b, h] >= S) & (lo < S)
+                gcut = val[win].min() if win.any() else np.inf
+            rows = set()
+            for j in bad:
+                a, c = sorted((int(g[b, h, j]), int(o[b, h, j])))
+                r0, r1 = max(a, int(lo[j])), min(c, S)
+                for i in range(r0, r1):
+                    checked += 1
+                    assert checked <= max_rows, "too many rows differ"
+                    if mode == 1:
+                        cut = gcut
+                    else:
+                        in_top = (lo <= i) & (i < o[b, h]) & (np.arange(S) <= i)
+                        cut = val[in_top].min() if in_top.any() else np.inf
+                    assert abs(val[j] - cut) <= TIE_TOL, \
+                        "key %d (b=%d h=%d) row %d: expiry gpu %d oracle %d, value %.9g cutoff %.9g" % (
+                            j, b, h, i, g[b, h, j], o[b, h, j], val[j], cut)
+                    rows.add(i)
+            affected[(b, h)] = rows
+    return affected
+
+
+def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 128, tiles=None):
+    """Per (b, h, tile): the gathered key list and the 64-key occupancy bitmap,
+    derived from the oracle's intervals by their definitions."""
+    o = or_ex.cpu().numpy()
+    B, Hkv, S = o.shape
+    lo = top_lo(S, block)
+    j = np.arange(S)
+    n_qt = (S + q_tile - 1) // q_tile
+    words = ((S + 63) // 64 + 31) // 32
+    lists, bitmaps = {}, {}
+    for b in range(B):
+        for h in range(Hkv):
+            e = o[b, h]
+            for t in (range(n_qt) if tiles is None else tiles):
+                q0, q1 = t * q_tile, min(S, (t + 1) * q_tile) - 1
+                lim = q0 - window if window > 0 else q1
+                top = (lo <= q1) & (e > q0) & (np.maximum(q0, lo) <= np.minimum(q1, e - 1))
+                lists[(b, h, t)] = j[top & (j <= lim)]
+                occ = top.copy()
+                if window > 0:
+                    occ |= (j <= q1) & (j > q0 - window)
+                bits = np.zeros(words, dtype=np.uint32)
+                blk = np.unique(j[occ] // 64)
+                np.bitwise_or.at(bits, blk // 32, (np.uint32(1) << (blk % 32).astype(np.uint32)))
+                bitmaps[(b, h, t)] = bits
+    return lists, bitmaps
+
+
+def check_outputs(O_gpu: torch.Tensor, O_ref: torch.Tensor, lse_gpu, lse_ref, rows, dtype, H: int, Hkv: int,
+                  affected=None):
+    """O_gpu [B][S][H][D] (all rows), O_ref [B][n_rows][H][D] for `rows`;
+    lse_gpu [B][H][S], lse_ref [B][H][n_rows]."""
+    tol = TOL[dtype]
+    G = H // Hkv
+    rows_t = torch.tensor(rows, dtype=torch.long)
+    g = O_gpu.double().cpu()[:, rows_t]
+    keep = torch.ones(g.shape[0], len(rows), H, dtype=torch.bool)
+    if affected:
+        for (b, h), rs in affected.items():
+            for r_i, i in enumerate(rows):
+                if i in rs:
+                    keep[b, r_i, h * G:(h + 1) * G] = False
+    err = (g - O_ref).abs().amax(dim=-1)
+    err = torch.where(keep, err, torch.zeros_like(err))
+    assert float(err.max()) <= tol, "max |O - O_ref| = %.3g > %.3g" % (float(err.max()), tol)
+    if lse_gpu is not None:
+        lg = lse_gpu.double().cpu()[:, :, rows_t]
+        kl = keep.permute(0, 2, 1)
+        both_inf = torch.isneginf(lg) & torch.isneginf(lse_ref)
+        assert bool((both_inf | ~torch.isneginf(lse_ref) | ~kl).all()), "empty rows differ"
+        d = torch.where(both_inf | ~kl, torch.zeros_like(lg), (lg - lse_ref).abs())
+        assert float(d.max()) <= tol, "max |lse - lse_ref| = %.3g" % float(d.max())
+    return int((~keep).sum())
