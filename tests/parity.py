@@ -7,7 +7,10 @@
   the comparison grants.  Rows touched by a swap are left out of the output
   comparison (the oracle is never fed a GPU-derived set).
 * Outputs match within a max-abs error of 1e-4 (fp32 inputs) or 2e-2 (bf16),
-  for O and for lse.
+  for O and for lse.  A bf16 output is rounded once (round-to-nearest-even) from
+  the fp32 result; the bound applies to the arithmetic before that rounding, so
+  each bf16 element is also granted half a bf16 ulp of the reference value
+  (above |O| = 8 that half ulp alone is 0.031, more than 2e-2).
 """
 from __future__ import annotations
 
@@ -18,6 +21,21 @@ TIE_TOL = 1e-5
 TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
 SCORE_ATOL = 5e-5
 SCORE_RTOL = 1e-5
+
+
+def bf16_half_ulp(x: torch.Tensor) -> torch.Tensor:
+    """Half the bf16 spacing at |x| (8 significant bits): |x| in [2^(e-1), 2^e)
+    has spacing 2^(e-8)."""
+    _, e = torch.frexp(x.double().abs())
+    return torch.ldexp(torch.ones_like(x, dtype=torch.float64), (e - 9).to(torch.int32))
+
+
+def out_tol(ref: torch.Tensor, dtype) -> torch.Tensor:
+    """Per-element bound for an output of `dtype` against fp64 `ref`."""
+    t = torch.full_like(ref, TOL[dtype], dtype=torch.float64)
+    if dtype == torch.bfloat16:
+        t = t + bf16_half_ulp(ref)
+    return t
 
 
 def top_lo(S: int, block: int) -> np.ndarray:
@@ -128,9 +146,9 @@ def check_outputs(O_gpu: torch.Tensor, O_ref: torch.Tensor, lse_gpu, lse_ref, ro
             for r_i, i in enumerate(rows):
                 if i in rs:
                     keep[b, r_i, h * G:(h + 1) * G] = False
-    err = (g - O_ref).abs().amax(dim=-1)
-    err = torch.where(keep, err, torch.zeros_like(err))
-    assert float(err.max()) <= tol, "max |O - O_ref| = %.3g > %.3g" % (float(err.max()), tol)
+    err = ((g - O_ref).abs() - out_tol(O_ref, dtype)).amax(dim=-1)
+    err = torch.where(keep, err, torch.full_like(err, -1.0))
+    assert float(err.max()) <= 0, "max |O - O_ref| exceeds its bound by %.3g" % float(err.max())
     if lse_gpu is not None:
         lg = lse_gpu.double().cpu()[:, :, rows_t]
         kl = keep.permute(0, 2, 1)
