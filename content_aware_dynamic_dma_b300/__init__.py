@@ -59,13 +59,15 @@ class KeptT(ctypes.Structure):
 
 
 EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_attn_prefill",
-            "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_get_device_status", "dma_status_string",
-            "dma_last_error_message", "dma_set_prefill_kernel", "dma_version")
+            "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_sparse_attn_decode_noalloc",
+            "dma_get_device_status", "dma_status_string", "dma_last_error_message", "dma_set_prefill_kernel",
+            "dma_version")
 
 
 def _load_lib():
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libdma.so is not built (%s); run: python -m content_aware_dynamic_dma_b300.build" % LIB_PATH)
+        raise ImportError("libdma.so is not built (%s); run: python content_aware_dynamic_dma_b300/build.py"
+                          % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     PK = ctypes.POINTER(KeptT)
@@ -76,6 +78,7 @@ def _load_lib():
         "dma_sparse_attn_prefill": [P, P, P, I, I, I, I, I, I, P, PK, F, P, P, P],
         "dma_decode_workspace_size": [I, I, I, I, I, I, ctypes.POINTER(Z)],
         "dma_sparse_attn_decode": [P, P, P, I, I, I, P, I, I, I, P, PK, F, P, P, P, Z, P],
+        "dma_sparse_attn_decode_noalloc": [P, P, P, I, I, I, P, I, I, I, P, PK, F, P, P, P],
         "dma_get_device_status": [P, ctypes.POINTER(I)],
         "dma_status_string": [I],
         "dma_last_error_message": [],
@@ -227,6 +230,20 @@ def dma_sparse_attn_decode(q: torch.Tensor, Kc: torch.Tensor, Vc: torch.Tensor, 
     _check(_lib.dma_sparse_attn_decode(_ptr(q), _ptr(Kc), _ptr(Vc), _dtype(q), B, Lmax, _ptr(cache_len), H, Hkv, D,
                                        _ptr(scores), ctypes.byref(kept.t), float(scale), _ptr(o), _ptr(lse),
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dma_sparse_attn_decode_noalloc(q: torch.Tensor, Kc: torch.Tensor, Vc: torch.Tensor, scores: torch.Tensor,
+                                   kept: Kept, o: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                                   cache_len: Optional[torch.Tensor] = None, scale: float = 0.0,
+                                   stream=None) -> None:
+    """dma_sparse_attn_decode for callers that cannot allocate: its scratch is a
+    fixed 64 MiB device array inside the library, shared by all calls on a
+    device (serialise calls that could overlap on the GPU)."""
+    B, H, D = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    _check(_lib.dma_sparse_attn_decode_noalloc(_ptr(q), _ptr(Kc), _ptr(Vc), _dtype(q), B, Lmax, _ptr(cache_len), H,
+                                               Hkv, D, _ptr(scores), ctypes.byref(kept.t), float(scale), _ptr(o),
+                                               _ptr(lse), _stream(stream)))
 
 
 def dma_get_device_status(stream=None) -> int:

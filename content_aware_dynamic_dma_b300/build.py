@@ -2,7 +2,9 @@
 
 Each ``csrc/*.cu`` compiles to an object under ``_build/`` (rebuilt when it or
 a header is newer), then the objects link into ``libdma.so`` beside this file.
-Run ``python -m content_aware_dynamic_dma_b300.build`` or call ``build()``.
+Run it as a script, ``python content_aware_dynamic_dma_b300/build.py``, or
+through ``__graft_entry__.build()`` (importing the package loads the library,
+so the package import cannot be the way to build it).
 """
 from __future__ import annotations
 

@@ -14,6 +14,7 @@
 // the group, a chunk-local softmax and the partial output.  A second kernel
 // merges the chunks of each (sequence, query head) by their log-sum-exp.
 #include <cmath>
+#include <mutex>
 
 #include "dma_internal.cuh"
 
@@ -264,3 +265,63 @@ cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, dma_dty
 }
 
 }  // namespace dma
+
+// ------------------------------------------------ decode without allocation --
+//
+// Some callers cannot call cudaMalloc at all: a serving loop that runs on a
+// fixed memory plan, an embedding host library that has no access to the
+// application's allocator, or code that may not trigger the device-wide
+// synchronisation an allocation can imply.  For them the decode split-K
+// partials live in this file-scope device array instead of a caller-provided
+// workspace.  Every GPU that loads the library holds the array until the
+// process exits.
+namespace dma {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+void* g_scratch_addr[kNoAllocMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+}  // namespace
+
+}  // namespace dma
+
+extern "C" dma_status_t dma_sparse_attn_decode_noalloc(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt,
+                                                       int B, int Lmax, const int32_t* cache_len, int H, int Hkv,
+                                                       int D, const float* scores, const dma_kept_t* kept,
+                                                       float scale, void* o, float* lse, dma_stream_t stream)
+{
+    using namespace dma;
+    if (!kept) return set_error(DMA_ERR_INVALID_ARG, "kept is NULL");
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || kept->top_cap < 0 || kept->window < 0)
+        return set_error(DMA_ERR_INVALID_ARG, "bad sizes B=%d H=%d Hkv=%d", B, H, Hkv);
+    if (D != 64 && D != 128) return set_error(DMA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+    const size_t need = decode_ws_bytes(B, H, Hkv, D, kept->top_cap, kept->window);
+    if (need > kNoAllocScratchBytes)
+        return set_error(DMA_ERR_UNSUPPORTED,
+                         "decode_noalloc needs %zu bytes of scratch, more than its fixed %zu; use "
+                         "dma_sparse_attn_decode with a workspace", need, kNoAllocScratchBytes);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(DMA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(DMA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    void* scratch = nullptr;
+    {
+        // first call on this device: look up the array's device address with the
+        // device current (the host-side name is only a stand-in for it)
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess)
+                return set_error(DMA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+            g_scratch_addr[dev] = p;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    return dma_sparse_attn_decode(q, Kc, Vc, dt, B, Lmax, cache_len, H, Hkv, D, scores, kept, scale, o, lse,
+                                  scratch, kNoAllocScratchBytes, stream);
+}

@@ -98,6 +98,16 @@ dma_status_t check_kept_geometry(const dma_kept_t* kept, int B, int Hkv, int S)
 }
 
 }  // namespace
+
+dma_status_t set_error(dma_status_t s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
 }  // namespace dma
 
 using namespace dma;

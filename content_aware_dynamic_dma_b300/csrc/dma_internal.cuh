@@ -50,6 +50,10 @@ struct SelectPlan {
 
 SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block);
 
+// Records the per-thread detail message returned by dma_last_error_message()
+// and returns `s`.
+dma_status_t set_error(dma_status_t s, const char* fmt, ...);
+
 // ---- launchers (host) -----------------------------------------------------
 
 cudaError_t launch_score(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,

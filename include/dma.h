@@ -182,6 +182,32 @@ dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* V
                                     const dma_kept_t* kept, float scale, void* o, float* lse, void* ws,
                                     size_t ws_bytes, dma_stream_t stream);
 
+/* Decode for callers that cannot allocate device memory.  The method has no
+ * counterpart for this call; it exists for callers that may not call cudaMalloc
+ * at all -- a serving loop running on a fixed memory plan, a host library with
+ * no access to the application's allocator, or code that must not risk the
+ * device-wide synchronisation an allocation can cause.
+ *
+ * Same arguments and result as dma_sparse_attn_decode, without the workspace:
+ * the split-K partials go to a 64 MiB array that the library holds in device
+ * memory on every GPU that loads it, until the process exits.  The call itself
+ * allocates nothing.
+ *   - Limit: when the partials would need more than 64 MiB
+ *     (4 * B * H * ceil((top_cap + window) / 64) * (D + 2) + 256 bytes), the call
+ *     returns DMA_ERR_UNSUPPORTED before launching anything.
+ *   - Set-up: the first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - Sharing: all calls on a device use the same array, which keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls that overlap
+ *     on the GPU -- on different streams, or from different threads -- race on
+ *     it and must be serialised by the caller.
+ */
+dma_status_t dma_sparse_attn_decode_noalloc(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B,
+                                            int Lmax, const int32_t* cache_len, int H, int Hkv, int D,
+                                            const float* scores, const dma_kept_t* kept, float scale, void* o,
+                                            float* lse, dma_stream_t stream);
+
 /* ------------------------------------------------------------------ misc -- */
 
 /* Synchronises `stream`, returns the device status word (a dma_status_t value,

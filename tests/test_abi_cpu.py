@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def dma():
-    from content_aware_dynamic_dma_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import content_aware_dynamic_dma_b300 as d
     return d
 
