@@ -363,8 +363,12 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=PREFILL_WL, choices=[PREFILL_WL, "prefill_s64k_block64_bf16"])
+    ap.add_argument("--workload", default=PREFILL_WL,
+                    choices=[PREFILL_WL, "prefill_s64k_block64_bf16", "prefill_s16k_bf16", "prefill_s4k_gqa_bf16"],
+                    help="prefill workload of a step (the smaller ones serve profiling runs)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode only (a profiling aid: the line then carries no prefill metric)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=1024, help="rows per (b, head) in the CPU-baseline sample")
@@ -382,6 +386,13 @@ def main():
     world, rank, local = dist_setup()
     peaks = load_peaks()
     clocks = ClockSampler(local)
+    if args.no_prefill:
+        dec = bench_decode(args, world)
+        if rank == 0:
+            print(json.dumps({"metric": "decode selected-KV GB/s", "value": round(dec["gbs"], 2), "unit": "GB/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "decode": dec}), flush=True)
+        return
     pf = bench_prefill(args, world, rank, peaks, clocks)
     dec = None if args.no_decode else bench_decode(args, world)
 

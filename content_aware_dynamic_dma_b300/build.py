@@ -60,7 +60,7 @@ def build(verbose: bool = False, extra=None) -> str:
         objs = list(ex.map(lambda s: _compile(s, extra), srcs))
     if _stale(LIB, objs):
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcuda"]
+        cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stdout + r.stderr))

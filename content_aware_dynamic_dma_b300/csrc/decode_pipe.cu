@@ -1,0 +1,457 @@
+// Sparse attention decode, bf16: a pipelined split-K kernel over the kept rows.
+//
+// Dynamic Mask Attention summary (lsdiaocha.cn), §七: the full KV cache stays
+// resident and only the selection changes; row L-1 of a cache of length L
+// attends to the top set of that row united with the window {L-window .. L-1}.
+// Skipped rows are never read (§四).
+//
+// HBM-bound: the algorithmic traffic is 2 * D * 2 bytes of K and V per kept row
+// per KV head.  One CTA takes a contiguous part of one (sequence, KV head)
+// kept list.  A producer warp gathers the K and V rows of 64 kept keys per
+// stage with TMA (tile::gather4, four rows per instruction) into three stages
+// of shared memory, so several stages are in flight while the four consumer
+// warps work.  Each consumer warp takes 16 keys of a stage: logits of all
+// G = H / Hkv query heads of the group with mma.sync (query heads padded to
+// 16 rows, keys as the 8-wide N dimension), an online softmax in the log2
+// domain in registers, and O += P V with P taken straight from the logit
+// accumulators.  The warps' partial results are merged in shared memory and
+// written as one (max, sum, O) partial per (sequence, query head, split); a
+// second kernel merges the splits by log-sum-exp.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "dma_internal.cuh"
+#include "tc_primitives.cuh"
+
+namespace dma {
+namespace {
+
+using namespace tc;
+
+constexpr int kStageKeys = 64;
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct PipeLayout {
+    static constexpr int kHalf = kStageKeys * 128;      // one 64-column half of a 64-row tile
+    static constexpr int kTile = kStageKeys * D * 2;    // K or V rows of one stage
+    static constexpr int kStage = 2 * kTile;            // K then V
+    static constexpr int kBias = kStages * kStage;      // [stage][64] f32
+    static constexpr int kMerge = 0;  // [warp][16][D + 2] f32, over the stages once the pipeline is drained
+    static_assert(kConsumerWarps * 16 * (D + 2) * 4 <= kBias, "merge area must fit in the stages");
+    static constexpr int kBars = kBias + kStages * kStageKeys * 4;
+    static constexpr int kMisc = kBars + 8 * 2 * kStages;
+    static constexpr int kEnd = kMisc + 16;
+    static constexpr int kSmemBytes = kEnd + 1024;
+};
+
+struct PipeArgs {
+    const __nv_bfloat16* q;     // [B][H][D]
+    const int32_t* cache_len;   // [B] or null
+    const float* scores;        // [B][Hkv][Lmax]
+    const int32_t* top_idx;     // [B][Hkv][top_cap]
+    const int32_t* top_count;   // [B][Hkv]
+    float* part_o;              // [B * H][nsplit][D]
+    float* part_ml;             // [B * H][nsplit][2]  (max in log2 units, sum)
+    int* status;
+    int B, Lmax, H, Hkv, G, top_cap, window, nsplit;
+    float c_log2;               // scale * log2(e)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D (16x8, f32) += A (16x16, bf16, row) * B (16x8, bf16, col)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of the 16-byte chunk `chunk` (8 elements) of row r in a
+// 128-byte-swizzled tile of 64 rows.
+__device__ __forceinline__ uint32_t sw_off(int r, int chunk)
+{
+    return (uint32_t)((chunk >> 3) * (kStageKeys * 128) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+}
+
+// Entry u of the (sequence, KV head) list: top-set keys outside the window,
+// then the window band; -1 for an entry that contributes nothing.
+__device__ __forceinline__ int list_key(int u, const int32_t* top, int n_top, int L, int window)
+{
+    if (u < n_top) {
+        const int j = top[u];
+        return (j >= 0 && j < L - window && j <= L - 1) ? j : -1;
+    }
+    const int j = L - window + (u - n_top);
+    return (j >= 0 && j <= L - 1) ? j : -1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPipeThreads) decode_pipe_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap vmap,
+                                                                   const PipeArgs a)
+{
+    using L_ = PipeLayout<D>;
+    constexpr int kNT = D / 8;      // 8-wide output tiles
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    float* bias_s = reinterpret_cast<float*>(sm + L_::kBias);
+    float* merge_s = reinterpret_cast<float*>(sm + L_::kMerge);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L_::kMisc);
+    auto full_bar = [&](int s) { return sbase + L_::kBars + 8 * s; };
+    auto empty_bar = [&](int s) { return sbase + L_::kBars + 8 * (kStages + s); };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = blockIdx.y, split = blockIdx.x;
+    const int b = seg / a.Hkv, h = seg % a.Hkv;
+    const int G = a.G;
+    // cache lengths outside [1, Lmax] are clamped so that no row outside the cache is read
+    const int L = a.cache_len ? min(max(a.cache_len[b], 1), a.Lmax) : a.Lmax;
+    const int n_top = min(max(a.top_count[seg], 0), a.top_cap);
+    const int n_all = n_top + a.window;
+    const int per = ((n_all + a.nsplit - 1) / a.nsplit + kStageKeys - 1) / kStageKeys * kStageKeys;
+    const int u_begin = min(n_all, split * per), u_end = min(n_all, u_begin + per);
+    const int nst = (u_end - u_begin + kStageKeys - 1) / kStageKeys;
+    const int32_t* top = a.top_idx + (int64_t)seg * a.top_cap;
+    const float* sc = a.scores + (int64_t)seg * a.Lmax;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 32);
+            mbar_init(empty_bar(s), kConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const int64_t row0 = (int64_t)b * a.Lmax * a.Hkv + h;
+        const bool is_v = lane >= 16;
+        const int r4 = 4 * (lane & 15);
+        int issued = 0;
+        for (int st = 0; st < nst; ++st) {
+            const int s = st % kStages, use = st / kStages;
+            if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait(empty_bar(s), (use - 1) & 1, abort_flag, kWaitNs))) break;
+            int rr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int u = u_begin + st * kStageKeys + r4 + e;
+                const int j = u < u_end ? list_key(u, top, n_top, L, a.window) : -1;
+                rr[e] = j >= 0 ? (int)(row0 + (int64_t)j * a.Hkv) : -1;
+                if (!is_v) bias_s[s * kStageKeys + r4 + e] = j >= 0 ? sc[j] * kLog2e : -INFINITY;
+            }
+            if (lane == 0)
+                mbar_arrive_expect_tx(full_bar(s), 2 * L_::kTile);
+            else
+                mbar_arrive(full_bar(s));
+            const uint32_t dst = sbase + s * L_::kStage + (is_v ? L_::kTile : 0) + r4 * 128;
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf)
+                tma_gather4(dst + hf * L_::kHalf, is_v ? &vmap : &kmap, 64 * hf, rr[0], rr[1], rr[2], rr[3],
+                            full_bar(s));
+            issued = st + 1;
+        }
+        if (*abort_flag) {
+            // let the gathers already issued land before shared memory is given up
+            for (int st = max(0, issued - kStages); st < issued; ++st)
+                mbar_wait_drain(full_bar(st % kStages), (st / kStages) & 1, kWaitNs);
+        }
+        __syncthreads();
+    } else {
+        // ----------------------------------------------------------- consumers
+        const int g = lane >> 2, t = lane & 3;
+        // query fragments (A operand, heads as rows): rows g and g + 8, dims 16 kk + 2 t (+1, +8, +9)
+        uint32_t qa[D / 16][4];
+        {
+            const __nv_bfloat16* qb = a.q + ((int64_t)b * a.H + (int64_t)h * G) * D;
+            auto qv = [&](int row, int d) -> uint32_t {
+                if (row >= G) return 0u;
+                return *reinterpret_cast<const uint32_t*>(qb + (int64_t)row * D + d);
+            };
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                qa[kk][0] = qv(g, 16 * kk + 2 * t);
+                qa[kk][1] = qv(g + 8, 16 * kk + 2 * t);
+                qa[kk][2] = qv(g, 16 * kk + 2 * t + 8);
+                qa[kk][3] = qv(g + 8, 16 * kk + 2 * t + 8);
+            }
+        }
+        float o[kNT][4];
+#pragma unroll
+        for (int n = 0; n < kNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g + 8
+        const int kr = 16 * warp;  // this warp's 16 keys of each stage
+        for (int st = 0; st < nst; ++st) {
+            const int s = st % kStages;
+            // the outcome is made warp-uniform: ldmatrix and mma.sync below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), (st / kStages) & 1, abort_flag, kWaitNs))) break;
+            const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
+            // logits: two 8-key tiles
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const int key = kr + 8 * (mi >> 1) + ri;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kt + sw_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                    mma16816(c0, qa[kk], b0, b1);
+                    mma16816(c1, qa[kk], b2, b3);
+                }
+            }
+            const float* bs = bias_s + s * kStageKeys + kr;
+            const float bb0 = bs[2 * t], bb1 = bs[2 * t + 1], bb2 = bs[8 + 2 * t], bb3 = bs[8 + 2 * t + 1];
+            // x for head g: c0[0], c0[1], c1[0], c1[1]; head g + 8: c0[2], c0[3], c1[2], c1[3]
+            float x0 = fmaf(c0[0], a.c_log2, bb0), x1 = fmaf(c0[1], a.c_log2, bb1);
+            float x2 = fmaf(c1[0], a.c_log2, bb2), x3 = fmaf(c1[1], a.c_log2, bb3);
+            float y0 = fmaf(c0[2], a.c_log2, bb0), y1 = fmaf(c0[3], a.c_log2, bb1);
+            float y2 = fmaf(c1[2], a.c_log2, bb2), y3 = fmaf(c1[3], a.c_log2, bb3);
+            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+            my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+            const float mn0 = fmaxf(m0, mx), mn1 = fmaxf(m1, my);
+            const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2(m0 - e0), al1 = ex2(m1 - e1);  // 0 while nothing was kept
+            m0 = mn0;
+            m1 = mn1;
+            x0 = ex2(x0 - e0);
+            x1 = ex2(x1 - e0);
+            x2 = ex2(x2 - e0);
+            x3 = ex2(x3 - e0);
+            y0 = ex2(y0 - e1);
+            y1 = ex2(y1 - e1);
+            y2 = ex2(y2 - e1);
+            y3 = ex2(y3 - e1);
+            float s0 = (x0 + x1) + (x2 + x3), s1 = (y0 + y1) + (y2 + y3);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            l0 = l0 * al0 + s0;
+            l1 = l1 * al1 + s1;
+            const uint32_t pa[4] = {pack_bf16(x0, x1), pack_bf16(y0, y1), pack_bf16(x2, x3), pack_bf16(y2, y3)};
+            // O += P V: V fragments by transposed 8x8 loads, two 8-wide output tiles per load
+            {
+                const int mi = lane >> 3, ri = lane & 7;
+                const int key = kr + 8 * (mi & 1) + ri;
+#pragma unroll
+                for (int n = 0; n < kNT; n += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vt + sw_off(key, n + (mi >> 1)), b0, b1, b2, b3);
+                    o[n][0] *= al0;
+                    o[n][1] *= al0;
+                    o[n][2] *= al1;
+                    o[n][3] *= al1;
+                    o[n + 1][0] *= al0;
+                    o[n + 1][1] *= al0;
+                    o[n + 1][2] *= al1;
+                    o[n + 1][3] *= al1;
+                    mma16816(o[n], pa, b0, b1);
+                    mma16816(o[n + 1], pa, b2, b3);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
+        }
+        // every warp is done with the stages before they are reused for the merge
+        __syncthreads();
+        // this warp's partial: rows g (and g + 8) of (m, l, O)
+        float* mw = merge_s + warp * 16 * (D + 2);
+        if (t == 0) {
+            mw[g * (D + 2) + D] = m0;
+            mw[g * (D + 2) + D + 1] = l0;
+            mw[(g + 8) * (D + 2) + D] = m1;
+            mw[(g + 8) * (D + 2) + D + 1] = l1;
+        }
+#pragma unroll
+        for (int n = 0; n < kNT; ++n) {
+            mw[g * (D + 2) + 8 * n + 2 * t] = o[n][0];
+            mw[g * (D + 2) + 8 * n + 2 * t + 1] = o[n][1];
+            mw[(g + 8) * (D + 2) + 8 * n + 2 * t] = o[n][2];
+            mw[(g + 8) * (D + 2) + 8 * n + 2 * t + 1] = o[n][3];
+        }
+    }
+    __syncthreads();
+    // merge the consumer warps and write this split's partial for each query head
+    for (int e = threadIdx.x; e < G * (D + 2); e += kPipeThreads) {
+        const int hg = e / (D + 2), c = e % (D + 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_s[(w * 16 + hg) * (D + 2) + D]);
+        float acc = 0.f;
+        if (M != -INFINITY) {
+            const int cc = c == D ? D + 1 : c;  // the max slot merges the sums
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = merge_s[(w * 16 + hg) * (D + 2) + D];
+                if (mw != -INFINITY) acc = fmaf(merge_s[(w * 16 + hg) * (D + 2) + cc], ex2(mw - M), acc);
+            }
+        }
+        const int64_t pi = ((int64_t)b * a.H + (int64_t)h * G + hg) * a.nsplit + split;
+        if (c < D)
+            a.part_o[pi * D + c] = acc;
+        else if (c == D)
+            a.part_ml[pi * 2 + 1] = acc;
+        else
+            a.part_ml[pi * 2] = M;
+    }
+    if (threadIdx.x == 0 && *abort_flag) set_status(a.status, DMA_ERR_TIMEOUT);
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) decode_pipe_merge_kernel(int nsplit, const float* __restrict__ part_o,
+                                                              const float* __restrict__ part_ml,
+                                                              __nv_bfloat16* __restrict__ o, float* __restrict__ lse)
+{
+    const int bh = blockIdx.x, d = threadIdx.x;
+    const float* ml = part_ml + (int64_t)bh * nsplit * 2;
+    float M = -INFINITY;
+    for (int c = 0; c < nsplit; ++c) M = fmaxf(M, ml[2 * c]);
+    float Ls = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+        for (int c = 0; c < nsplit; ++c) {
+            const float mc = ml[2 * c];
+            if (mc == -INFINITY) continue;
+            const float wgt = ex2(mc - M);
+            Ls = fmaf(ml[2 * c + 1], wgt, Ls);
+            acc = fmaf(part_o[((int64_t)bh * nsplit + c) * D + d], wgt, acc);
+        }
+    }
+    o[(int64_t)bh * D + d] = __float2bfloat16_rn(Ls > 0.f ? acc / Ls : 0.f);
+    if (lse && d == 0) lse[bh] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int D)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, int Lmax, const int32_t* cache_len,
+                         int H, int Hkv, const float* scores, const dma_kept_t* kept, float scale, void* o,
+                         float* lse, void* ws, int nsplit, int* status, cudaStream_t st)
+{
+    CUtensorMap km, vm;
+    if (!make_rows_map(&km, Kc, (int64_t)B * Lmax * Hkv, D) || !make_rows_map(&vm, Vc, (int64_t)B * Lmax * Hkv, D))
+        return cudaErrorInvalidValue;
+    PipeArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.cache_len = cache_len;
+    a.scores = scores;
+    a.top_idx = kept->top_idx;
+    a.top_count = kept->top_count;
+    a.part_o = static_cast<float*>(ws);
+    a.part_ml = a.part_o + (size_t)B * H * nsplit * D;
+    a.status = status;
+    a.B = B;
+    a.Lmax = Lmax;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.G = H / Hkv;
+    a.top_cap = kept->top_cap;
+    a.window = kept->window;
+    a.nsplit = nsplit;
+    a.c_log2 = scale * kLog2e;
+    const int smem = PipeLayout<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(decode_pipe_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(km, vm, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    decode_pipe_merge_kernel<D><<<B * H, D, 0, st>>>(nsplit, a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(o), lse);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_pipe_supported(dma_dtype_t dt, int B, int Lmax, int H, int Hkv, int D)
+{
+    return dt == DMA_BF16 && (D == 64 || D == 128) && H / Hkv <= 16 && (int64_t)B * Lmax * Hkv < ((int64_t)1 << 31);
+}
+
+// Splits per (sequence, KV head): enough CTAs for about four waves of two per
+// SM, never more than the 64-row chunks of the longest list (the workspace is
+// sized for that many).
+int decode_pipe_splits(int B, int Hkv, int top_cap, int window)
+{
+    const int max_split = (top_cap + window + 63) / 64;
+    const int want = (4 * 2 * 148 + B * Hkv - 1) / (B * Hkv);
+    return std::max(1, std::min(max_split, want));
+}
+
+cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, int B, int Lmax,
+                               const int32_t* cache_len, int H, int Hkv, int D, const float* scores,
+                               const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, int* status,
+                               cudaStream_t st)
+{
+    const int nsplit = decode_pipe_splits(B, Hkv, kept->top_cap, kept->window);
+    if (D == 128)
+        return launch_typed<128>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kept, scale, o, lse, ws, nsplit,
+                                 status, st);
+    return launch_typed<64>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kept, scale, o, lse, ws, nsplit, status,
+                            st);
+}
+
+}  // namespace dma

@@ -263,7 +263,14 @@ dma_status_t dma_sparse_attn_prefill(const void* Q, const void* K, const void* V
         return fail(DMA_ERR_INVALID_ARG, "prefill needs kept->expiry, tile_cnt and tile_idx");
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_prefill_simt(Q, K, V, dt, B, S, H, Hkv, D, scores, kept, scale, O, lse, st);
+    cudaError_t e;
+    if (g_prefill_kernel == 0 && prefill_tc_supported(dt, B, S, H, Hkv, D)) {
+        int* status = nullptr;
+        if ((s = status_ptr(&status)) != DMA_OK) return s;
+        e = launch_prefill_tc(Q, K, V, B, S, H, Hkv, D, scores, kept, scale, O, lse, status, st);
+    } else {
+        e = launch_prefill_simt(Q, K, V, dt, B, S, H, Hkv, D, scores, kept, scale, O, lse, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return ok();
 }
@@ -298,8 +305,16 @@ dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* V
         return fail(DMA_ERR_WORKSPACE, "decode workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0, need);
     if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
     if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
-    cudaError_t e = launch_decode(q, Kc, Vc, dt, B, Lmax, cache_len, H, Hkv, D, scores, kept, scale, o, lse, ws,
-                                  reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (decode_pipe_supported(dt, B, Lmax, H, Hkv, D)) {
+        int* status = nullptr;
+        if ((s = status_ptr(&status)) != DMA_OK) return s;
+        e = launch_decode_pipe(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, D, scores, kept, scale, o, lse, ws, status,
+                               reinterpret_cast<cudaStream_t>(stream));
+    } else {
+        e = launch_decode(q, Kc, Vc, dt, B, Lmax, cache_len, H, Hkv, D, scores, kept, scale, o, lse, ws,
+                          reinterpret_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return ok();
 }

@@ -68,6 +68,20 @@ cudaError_t launch_prefill_simt(const void* Q, const void* K, const void* V, dma
                                 int Hkv, int D, const float* scores, const dma_kept_t* kept, float scale, void* O,
                                 float* lse, cudaStream_t st);
 
+// Tensor-core prefill (bf16, D = 64 or 128).
+bool prefill_tc_supported(dma_dtype_t dt, int B, int S, int H, int Hkv, int D);
+cudaError_t launch_prefill_tc(const void* Q, const void* K, const void* V, int B, int S, int H, int Hkv, int D,
+                              const float* scores, const dma_kept_t* kept, float scale, void* O, float* lse,
+                              int* status, cudaStream_t st);
+
+// Pipelined bf16 decode (TMA row gathers, mma.sync, split-K).
+bool decode_pipe_supported(dma_dtype_t dt, int B, int Lmax, int H, int Hkv, int D);
+int decode_pipe_splits(int B, int Hkv, int top_cap, int window);
+cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, int B, int Lmax,
+                               const int32_t* cache_len, int H, int Hkv, int D, const float* scores,
+                               const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, int* status,
+                               cudaStream_t st);
+
 size_t decode_ws_bytes(int B, int H, int Hkv, int D, int top_cap, int window);
 cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
                           const int32_t* cache_len, int H, int Hkv, int D, const float* scores,

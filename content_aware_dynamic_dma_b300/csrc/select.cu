@@ -528,8 +528,12 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const int32_t*
 // ----------------------------------------------------------- per-tile lists ---
 
 constexpr int kTileThreads = 256;
+constexpr int kTilePartialCap = 1024;  // keys kept by only some rows of a tile (at most ~256 by construction)
 // For query tile [q0, q1]: keys j <= lim (lim = q0 - window, or q1 without a
-// window) with lo_j <= q1 and expiry_j > q0, ascending; plus the bitmap of
+// window) with lo_j <= q1 and expiry_j > q0.  The keys kept by every row of the
+// tile (lo_j <= q0 and expiry_j > q1) come first, ascending, then the keys kept
+// by only some of its rows, ascending: a consumer that walks the list in blocks
+// finds the blocks that need a per-row mask at the end.  Also the bitmap of
 // 64-key blocks holding a kept key (gathered keys and the window band).
 __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(const int32_t* __restrict__ expiry,
                                                                  const int32_t* __restrict__ idx,
@@ -541,6 +545,7 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(const int32_t* 
 {
     extern __shared__ uint32_t bm[];  // [bitmap_words]
     __shared__ int warp_buf[32];
+    __shared__ int part_s[kTilePartialCap];
     __shared__ int stop;
     const int seg = blockIdx.y, tile = blockIdx.x;
     const int q0 = tile * kQTile, q1 = min(S, q0 + kQTile) - 1;
@@ -553,35 +558,57 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(const int32_t* 
         for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bm[t] = 0;
     if (threadIdx.x == 0) stop = 0;
     __syncthreads();
-    int run = 0;
+    int run_full = 0, run_part = 0;
     for (int base = 0; base < n; base += kTileThreads) {
         const int u = base + threadIdx.x;
         int j = u < n ? li[u] : INT32_MAX;
-        int act = 0;
+        int act_full = 0, act_part = 0;
         if (j < 0 || (j >= S && j != INT32_MAX)) {
             set_status(status, DMA_ERR_DEVICE_CHECK);
             j = INT32_MAX;
         }
         if (j <= lim) {
-            int e = ex[j];
-            act = (top_lo(j, block) <= q1 && e > q0) ? 1 : 0;
+            const int e = ex[j], lo = top_lo(j, block);
+            if (lo <= q1 && e > q0) {
+                if (lo <= q0 && e > q1)
+                    act_full = 1;
+                else
+                    act_part = 1;
+            }
         }
         if (u < n && j > lim) stop = 1;  // the list is ascending: nothing later qualifies
-        int tot;
-        int before = block_exclusive_scan(act, warp_buf, &tot);
-        if (act) {
-            int o = run + before;
+        int tot_full, tot_part;
+        const int before_full = block_exclusive_scan(act_full, warp_buf, &tot_full);
+        const int before_part = block_exclusive_scan(act_part, warp_buf, &tot_part);
+        if (act_full) {
+            const int o = run_full + before_full;
             if (o < tile_stride)
                 out[o] = j;
             else
                 set_status(status, DMA_ERR_DEVICE_CHECK);
-            if (bitmap) atomicOr(&bm[j / (kBitmapBlock * 32)], 1u << ((j / kBitmapBlock) & 31));
         }
-        run += tot;
+        if (act_part) {
+            const int o = run_part + before_part;
+            if (o < kTilePartialCap)
+                part_s[o] = j;
+            else
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+        }
+        if (bitmap && (act_full | act_part)) atomicOr(&bm[j / (kBitmapBlock * 32)], 1u << ((j / kBitmapBlock) & 31));
+        run_full += tot_full;
+        run_part += tot_part;
         __syncthreads();
         if (stop) break;
     }
-    if (threadIdx.x == 0) tile_cnt[(int64_t)seg * n_qt + tile] = min(run, tile_stride);
+    run_part = min(run_part, kTilePartialCap);
+    for (int t = threadIdx.x; t < run_part; t += kTileThreads) {
+        const int o = run_full + t;
+        if (o < tile_stride)
+            out[o] = part_s[t];
+        else
+            set_status(status, DMA_ERR_DEVICE_CHECK);
+    }
+    if (threadIdx.x == 0) tile_cnt[(int64_t)seg * n_qt + tile] = min(run_full + run_part, tile_stride);
     if (bitmap) {
         if (window > 0) {
             const int band_lo = max(0, q0 - window + 1);

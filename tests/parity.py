@@ -105,8 +105,10 @@ def check_expiry(gpu_ex: torch.Tensor, or_ex: torch.Tensor, or_scores: torch.Ten
 
 
 def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 128, tiles=None):
-    """Per (b, h, tile): the gathered key list and the 64-key occupancy bitmap,
-    derived from the oracle's intervals by their definitions."""
+    """Per (b, h, tile): the gathered key list (keys kept by every row of the
+    tile first, then the keys kept by only some of its rows, each ascending) and
+    the 64-key occupancy bitmap, derived from the oracle's intervals by their
+    definitions."""
     o = or_ex.cpu().numpy()
     B, Hkv, S = o.shape
     lo = top_lo(S, block)
@@ -121,7 +123,10 @@ def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 1
                 q0, q1 = t * q_tile, min(S, (t + 1) * q_tile) - 1
                 lim = q0 - window if window > 0 else q1
                 top = (lo <= q1) & (e > q0) & (np.maximum(q0, lo) <= np.minimum(q1, e - 1))
-                lists[(b, h, t)] = j[top & (j <= lim)]
+                sel = top & (j <= lim)
+                every_row = (lo <= q0) & (e > q1)
+                # keys kept by every row of the tile first, then the rest, each ascending
+                lists[(b, h, t)] = np.concatenate([j[sel & every_row], j[sel & ~every_row]])
                 occ = top.copy()
                 if window > 0:
                     occ |= (j <= q1) & (j > q0 - window)

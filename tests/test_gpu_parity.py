@@ -116,6 +116,17 @@ EDGE = [
     (1, 640, 2, 1, 64, torch.float32, 200, 0, 64, 1),     # block units, global
     (1, 200, 2, 2, 64, torch.float32, 63, 16, 64, 0),     # block budget 0: window only
     (3, 1000, 6, 3, 128, torch.bfloat16, 100, 33, 1, 0),
+    # bf16 cases for the tensor-core kernel: GQA group sizes 1, 3 and 8 (one query head per
+    # pass, an odd last pass, four passes), one row, nothing kept at all, window only,
+    # global mode with empty rows, D = 64 blocks
+    (2, 260, 2, 2, 64, torch.bfloat16, 40, 0, 1, 0),
+    (1, 333, 3, 1, 128, torch.bfloat16, 64, 16, 1, 0),
+    (1, 517, 8, 1, 128, torch.bfloat16, 200, 50, 1, 0),
+    (1, 1, 2, 1, 128, torch.bfloat16, 4, 0, 1, 0),
+    (1, 200, 4, 2, 64, torch.bfloat16, 0, 0, 1, 0),
+    (1, 384, 4, 2, 128, torch.bfloat16, 0, 100, 1, 0),
+    (1, 450, 4, 2, 128, torch.bfloat16, 30, 0, 1, 1),
+    (1, 1100, 4, 2, 64, torch.bfloat16, 256, 64, 64, 0),
 ]
 
 
