@@ -371,7 +371,7 @@ def main():
                     help="decode only (a profiling aid: the line then carries no prefill metric)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="rows per (b, head) in the CPU-baseline sample")
+    ap.add_argument("--cpu-rows", type=int, default=4096, help="rows per (b, head) in the CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per (b, head) per reference-arm step")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -27,9 +27,11 @@
 // and 384.  The MMA order S_A(k+1) after PV_A(k), then PV_B(k), S_B(k+1) lets
 // one softmax warpgroup work while the tensor core serves the other.
 //
-// The running maximum is only moved when a block raises it by more than 8
-// (log2 units, a factor 256); otherwise exponents are taken against the old
-// maximum, which keeps P <= 256 and avoids rescaling O in tensor memory.
+// Exponents are always taken against the exact running maximum of the row, so
+// the largest weight seen so far is exactly 1.0 in bf16.  (Keeping an older
+// maximum until it is exceeded by a wide margin would save rescaling O in
+// tensor memory, but then the dominant weight of a peaked row is 2^f with a
+// fractional f, and its bf16 rounding alone moves O by up to 2^-9 |V|.)
 // Every wait is bounded (2 s); a wait that runs out sets DMA_ERR_TIMEOUT in the
 // device status word and the CTA winds down without further work.
 #include <cmath>
@@ -57,7 +59,7 @@ constexpr int kRegsSoftmax = 208;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.f;
+constexpr float kRescaleThreshold = 0.f;  // rescale whenever the row maximum rises
 // One exponential pair in kPolyEvery is computed by ex2_poly (0: none).
 constexpr int kPolyEvery = 0;
 
@@ -473,9 +475,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                // The maximum of a row moved up by more than 8: rescale what it has accumulated.
-                // tcgen05.ld/st are warp-collective, so the warp rescales together whenever one
-                // of its rows needs it (factor 1 for the others).
+                // The maximum of a row moved up: rescale what it has accumulated.  tcgen05.ld/st
+                // are warp-collective, so the warp rescales together whenever one of its rows
+                // needs it (factor 1 for the others).
                 const bool raise = m_blk > m_used + kRescaleThreshold;
                 const bool rescale = raise && k > 0 && m_used != -INFINITY;
                 const float alpha = rescale ? ex2(m_used - m_blk) : 1.f;
