@@ -7,18 +7,17 @@
 //
 // HBM-bound: the algorithmic traffic is 2 * D * 2 bytes of K and V per kept row
 // per KV head.  One CTA takes a contiguous part of one (sequence, KV head)
-// kept list.  A producer warp gathers the K and V rows of 64 kept keys per
-// stage with TMA (tile::gather4, four rows per instruction) into three stages
-// of shared memory, so several stages are in flight while the four consumer
-// warps work.  Each consumer warp takes 16 keys of a stage: logits of all
-// G = H / Hkv query heads of the group with mma.sync (query heads padded to
-// 16 rows, keys as the 8-wide N dimension), an online softmax in the log2
-// domain in registers, and O += P V with P taken straight from the logit
-// accumulators.  The warps' partial results are merged in shared memory and
-// written as one (max, sum, O) partial per (sequence, query head, split); a
-// second kernel merges the splits by log-sum-exp.
-#include <cudaTypedefs.h>
-
+// kept list and walks it in stages of 64 keys.  All four warps gather the K and
+// V rows of a stage with 16-byte cp.async copies (a TMA tile::gather4 moves only
+// about 8 bytes per cycle per SM, a quarter of what these row gathers need),
+// three stages in flight, into a 128-byte-swizzled layout.  Each warp then
+// takes 16 keys of the stage: logits of all G = H / Hkv query heads of the
+// group with mma.sync (query heads padded to 16 rows, keys as the 8-wide N
+// dimension), an online softmax in the log2 domain in registers, and
+// O += P V with P taken straight from the logit accumulators.  The warps'
+// partial results are merged in shared memory and written as one
+// (max, sum, O) partial per (sequence, query head, split); a second kernel
+// merges the splits by log-sum-exp.
 #include <algorithm>
 #include <cmath>
 
@@ -33,22 +32,18 @@ using namespace tc;
 constexpr int kStageKeys = 64;
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
-constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kPipeThreads = kConsumerWarps * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct PipeLayout {
-    static constexpr int kHalf = kStageKeys * 128;      // one 64-column half of a 64-row tile
     static constexpr int kTile = kStageKeys * D * 2;    // K or V rows of one stage
     static constexpr int kStage = 2 * kTile;            // K then V
     static constexpr int kBias = kStages * kStage;      // [stage][64] f32
     static constexpr int kMerge = 0;  // [warp][16][D + 2] f32, over the stages once the pipeline is drained
     static_assert(kConsumerWarps * 16 * (D + 2) * 4 <= kBias, "merge area must fit in the stages");
-    static constexpr int kBars = kBias + kStages * kStageKeys * 4;
-    static constexpr int kMisc = kBars + 8 * 2 * kStages;
-    static constexpr int kEnd = kMisc + 16;
+    static constexpr int kEnd = kBias + kStages * kStageKeys * 4;
     static constexpr int kSmemBytes = kEnd + 1024;
 };
 
@@ -60,7 +55,6 @@ struct PipeArgs {
     const int32_t* top_count;   // [B][Hkv]
     float* part_o;              // [B * H][nsplit][D]
     float* part_ml;             // [B * H][nsplit][2]  (max in log2 units, sum)
-    int* status;
     int B, Lmax, H, Hkv, G, top_cap, window, nsplit;
     float c_log2;               // scale * log2(e)
 };
@@ -122,21 +116,21 @@ __device__ __forceinline__ int list_key(int u, const int32_t* top, int n_top, in
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPipeThreads) decode_pipe_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                   const __grid_constant__ CUtensorMap vmap,
-                                                                   const PipeArgs a)
+__global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv_bfloat16* __restrict__ Kc,
+                                                                      const __nv_bfloat16* __restrict__ Vc,
+                                                                      const PipeArgs a)
 {
     using L_ = PipeLayout<D>;
-    constexpr int kNT = D / 8;      // 8-wide output tiles
+    constexpr int kNT = D / 8;       // 8-wide output tiles
+    constexpr int kCPR = D / 8;      // 16-byte chunks per row
+    constexpr int kRowsPerPass = kPipeThreads / kCPR;  // rows covered by one sweep of the CTA
+    constexpr int kSweeps = kStageKeys / kRowsPerPass;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
     float* bias_s = reinterpret_cast<float*>(sm + L_::kBias);
     float* merge_s = reinterpret_cast<float*>(sm + L_::kMerge);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L_::kMisc);
-    auto full_bar = [&](int s) { return sbase + L_::kBars + 8 * s; };
-    auto empty_bar = [&](int s) { return sbase + L_::kBars + 8 * (kStages + s); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.y, split = blockIdx.x;
@@ -151,152 +145,157 @@ __global__ void __launch_bounds__(kPipeThreads) decode_pipe_kernel(const __grid_
     const int nst = (u_end - u_begin + kStageKeys - 1) / kStageKeys;
     const int32_t* top = a.top_idx + (int64_t)seg * a.top_cap;
     const float* sc = a.scores + (int64_t)seg * a.Lmax;
+    const int64_t row_stride = (int64_t)a.Hkv * D;
+    const __nv_bfloat16* Kh = Kc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
+    const __nv_bfloat16* Vh = Vc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
 
-    if (threadIdx.x == 0) {
-        *abort_flag = 0;
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 32);
-            mbar_init(empty_bar(s), kConsumerWarps);
-        }
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------------ producer
-        const int64_t row0 = (int64_t)b * a.Lmax * a.Hkv + h;
-        const bool is_v = lane >= 16;
-        const int r4 = 4 * (lane & 15);
-        int issued = 0;
-        for (int st = 0; st < nst; ++st) {
-            const int s = st % kStages, use = st / kStages;
-            if (use >= 1 && !__all_sync(0xffffffffu, mbar_wait(empty_bar(s), (use - 1) & 1, abort_flag, kWaitNs))) break;
-            int rr[4];
+    // copy duty: chunk `part` of rows r0 + kRowsPerPass * m; bias of key threadIdx.x (< 64).
+    // The key indices of a stage are read one stage ahead of its copies, so the copies never
+    // wait for the index loads.
+    const int part = threadIdx.x % kCPR, r0 = threadIdx.x / kCPR;
+    struct StageKeys {
+        int j[kSweeps];
+        int jb;
+    };
+    auto keys_of = [&](int st) {
+        StageKeys k;
+        const int ub = u_begin + st * kStageKeys;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int u = u_begin + st * kStageKeys + r4 + e;
-                const int j = u < u_end ? list_key(u, top, n_top, L, a.window) : -1;
-                rr[e] = j >= 0 ? (int)(row0 + (int64_t)j * a.Hkv) : -1;
-                if (!is_v) bias_s[s * kStageKeys + r4 + e] = j >= 0 ? sc[j] * kLog2e : -INFINITY;
+        for (int m = 0; m < kSweeps; ++m) {
+            const int u = ub + r0 + kRowsPerPass * m;
+            k.j[m] = (st < nst && u < u_end) ? list_key(u, top, n_top, L, a.window) : -1;
+        }
+        const int ubb = ub + (int)threadIdx.x;
+        k.jb = (st < nst && threadIdx.x < kStageKeys && ubb < u_end) ? list_key(ubb, top, n_top, L, a.window) : -1;
+        return k;
+    };
+    auto issue = [&](int st, const StageKeys& k) {
+        if (st < nst) {
+            const int s = st % kStages;
+            const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
+#pragma unroll
+            for (int m = 0; m < kSweeps; ++m) {
+                const int r = r0 + kRowsPerPass * m;
+                const bool ok = k.j[m] >= 0;
+                const int64_t off = (int64_t)(ok ? k.j[m] : 0) * row_stride + part * 8;
+                cp_async16(kt + sw_off(r, part), Kh + off, ok);
+                cp_async16(vt + sw_off(r, part), Vh + off, ok);
             }
-            if (lane == 0)
-                mbar_arrive_expect_tx(full_bar(s), 2 * L_::kTile);
-            else
-                mbar_arrive(full_bar(s));
-            const uint32_t dst = sbase + s * L_::kStage + (is_v ? L_::kTile : 0) + r4 * 128;
+            if (threadIdx.x < kStageKeys) {
+                float* bd = bias_s + s * kStageKeys + threadIdx.x;
+                if (k.jb >= 0)
+                    cp_async4(smem_u32(bd), sc + k.jb);
+                else
+                    *bd = -INFINITY;
+            }
+        }
+        cp_async_commit();  // one group per stage slot, possibly empty, so the group count stays uniform
+    };
+
+    const int g = lane >> 2, t = lane & 3;
+    // query fragments (A operand, heads as rows): rows g and g + 8, dims 16 kk + 2 t (+1, +8, +9)
+    uint32_t qa[D / 16][4];
+    {
+        const __nv_bfloat16* qb = a.q + ((int64_t)b * a.H + (int64_t)h * G) * D;
+        auto qv = [&](int row, int d) -> uint32_t {
+            if (row >= G) return 0u;
+            return *reinterpret_cast<const uint32_t*>(qb + (int64_t)row * D + d);
+        };
 #pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf)
-                tma_gather4(dst + hf * L_::kHalf, is_v ? &vmap : &kmap, 64 * hf, rr[0], rr[1], rr[2], rr[3],
-                            full_bar(s));
-            issued = st + 1;
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qa[kk][0] = qv(g, 16 * kk + 2 * t);
+            qa[kk][1] = qv(g + 8, 16 * kk + 2 * t);
+            qa[kk][2] = qv(g, 16 * kk + 2 * t + 8);
+            qa[kk][3] = qv(g + 8, 16 * kk + 2 * t + 8);
         }
-        if (*abort_flag) {
-            // let the gathers already issued land before shared memory is given up
-            for (int st = max(0, issued - kStages); st < issued; ++st)
-                mbar_wait_drain(full_bar(st % kStages), (st / kStages) & 1, kWaitNs);
-        }
-        __syncthreads();
-    } else {
-        // ----------------------------------------------------------- consumers
-        const int g = lane >> 2, t = lane & 3;
-        // query fragments (A operand, heads as rows): rows g and g + 8, dims 16 kk + 2 t (+1, +8, +9)
-        uint32_t qa[D / 16][4];
+    }
+    float o[kNT][4];
+#pragma unroll
+    for (int n = 0; n < kNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g + 8
+    const int kr = 16 * warp;  // this warp's 16 keys of each stage
+
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) issue(st, keys_of(st));
+    StageKeys next = keys_of(kStages - 1);
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<kStages - 2>();  // this thread's copies of stage st have landed
+        __syncthreads();               // everyone's have; everyone is done with stage st - 1
+        issue(st + kStages - 1, next);  // into the slot of stage st - 1
+        next = keys_of(st + kStages);
+        const int s = st % kStages;
+        const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
+        // logits: two 8-key tiles
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            const __nv_bfloat16* qb = a.q + ((int64_t)b * a.H + (int64_t)h * G) * D;
-            auto qv = [&](int row, int d) -> uint32_t {
-                if (row >= G) return 0u;
-                return *reinterpret_cast<const uint32_t*>(qb + (int64_t)row * D + d);
-            };
+            const int mi = lane >> 3, ri = lane & 7;
+            const int key = kr + 8 * (mi >> 1) + ri;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                qa[kk][0] = qv(g, 16 * kk + 2 * t);
-                qa[kk][1] = qv(g + 8, 16 * kk + 2 * t);
-                qa[kk][2] = qv(g, 16 * kk + 2 * t + 8);
-                qa[kk][3] = qv(g + 8, 16 * kk + 2 * t + 8);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kt + sw_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                mma16816(c0, qa[kk], b0, b1);
+                mma16816(c1, qa[kk], b2, b3);
             }
         }
-        float o[kNT][4];
+        const float* bs = bias_s + s * kStageKeys + kr;
+        const float bb0 = bs[2 * t], bb1 = bs[2 * t + 1], bb2 = bs[8 + 2 * t], bb3 = bs[8 + 2 * t + 1];
+        // x for head g: c0[0], c0[1], c1[0], c1[1]; head g + 8: c0[2], c0[3], c1[2], c1[3]
+        float x0 = fmaf(c0[0], a.c_log2, bb0 * kLog2e), x1 = fmaf(c0[1], a.c_log2, bb1 * kLog2e);
+        float x2 = fmaf(c1[0], a.c_log2, bb2 * kLog2e), x3 = fmaf(c1[1], a.c_log2, bb3 * kLog2e);
+        float y0 = fmaf(c0[2], a.c_log2, bb0 * kLog2e), y1 = fmaf(c0[3], a.c_log2, bb1 * kLog2e);
+        float y2 = fmaf(c1[2], a.c_log2, bb2 * kLog2e), y3 = fmaf(c1[3], a.c_log2, bb3 * kLog2e);
+        float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
+        my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
+        const float mn0 = fmaxf(m0, mx), mn1 = fmaxf(m1, my);
+        const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = ex2(m0 - e0), al1 = ex2(m1 - e1);  // 0 while nothing was kept
+        m0 = mn0;
+        m1 = mn1;
+        x0 = ex2(x0 - e0);
+        x1 = ex2(x1 - e0);
+        x2 = ex2(x2 - e0);
+        x3 = ex2(x3 - e0);
+        y0 = ex2(y0 - e1);
+        y1 = ex2(y1 - e1);
+        y2 = ex2(y2 - e1);
+        y3 = ex2(y3 - e1);
+        float s0 = (x0 + x1) + (x2 + x3), s1 = (y0 + y1) + (y2 + y3);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        l0 = l0 * al0 + s0;
+        l1 = l1 * al1 + s1;
+        const uint32_t pa[4] = {pack_bf16(x0, x1), pack_bf16(y0, y1), pack_bf16(x2, x3), pack_bf16(y2, y3)};
+        // O += P V: V fragments by transposed 8x8 loads, two 8-wide output tiles per load
+        {
+            const int mi = lane >> 3, ri = lane & 7;
+            const int key = kr + 8 * (mi & 1) + ri;
 #pragma unroll
-        for (int n = 0; n < kNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g + 8
-        const int kr = 16 * warp;  // this warp's 16 keys of each stage
-        for (int st = 0; st < nst; ++st) {
-            const int s = st % kStages;
-            // the outcome is made warp-uniform: ldmatrix and mma.sync below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(full_bar(s), (st / kStages) & 1, abort_flag, kWaitNs))) break;
-            const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
-            // logits: two 8-key tiles
-            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-            {
-                const int mi = lane >> 3, ri = lane & 7;
-                const int key = kr + 8 * (mi >> 1) + ri;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kt + sw_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                    mma16816(c0, qa[kk], b0, b1);
-                    mma16816(c1, qa[kk], b2, b3);
-                }
+            for (int n = 0; n < kNT; n += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vt + sw_off(key, n + (mi >> 1)), b0, b1, b2, b3);
+                o[n][0] *= al0;
+                o[n][1] *= al0;
+                o[n][2] *= al1;
+                o[n][3] *= al1;
+                o[n + 1][0] *= al0;
+                o[n + 1][1] *= al0;
+                o[n + 1][2] *= al1;
+                o[n + 1][3] *= al1;
+                mma16816(o[n], pa, b0, b1);
+                mma16816(o[n + 1], pa, b2, b3);
             }
-            const float* bs = bias_s + s * kStageKeys + kr;
-            const float bb0 = bs[2 * t], bb1 = bs[2 * t + 1], bb2 = bs[8 + 2 * t], bb3 = bs[8 + 2 * t + 1];
-            // x for head g: c0[0], c0[1], c1[0], c1[1]; head g + 8: c0[2], c0[3], c1[2], c1[3]
-            float x0 = fmaf(c0[0], a.c_log2, bb0), x1 = fmaf(c0[1], a.c_log2, bb1);
-            float x2 = fmaf(c1[0], a.c_log2, bb2), x3 = fmaf(c1[1], a.c_log2, bb3);
-            float y0 = fmaf(c0[2], a.c_log2, bb0), y1 = fmaf(c0[3], a.c_log2, bb1);
-            float y2 = fmaf(c1[2], a.c_log2, bb2), y3 = fmaf(c1[3], a.c_log2, bb3);
-            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)), my = fmaxf(fmaxf(y0, y1), fmaxf(y2, y3));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 1));
-            my = fmaxf(my, __shfl_xor_sync(0xffffffffu, my, 2));
-            const float mn0 = fmaxf(m0, mx), mn1 = fmaxf(m1, my);
-            const float e0 = mn0 == -INFINITY ? 0.f : mn0, e1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = ex2(m0 - e0), al1 = ex2(m1 - e1);  // 0 while nothing was kept
-            m0 = mn0;
-            m1 = mn1;
-            x0 = ex2(x0 - e0);
-            x1 = ex2(x1 - e0);
-            x2 = ex2(x2 - e0);
-            x3 = ex2(x3 - e0);
-            y0 = ex2(y0 - e1);
-            y1 = ex2(y1 - e1);
-            y2 = ex2(y2 - e1);
-            y3 = ex2(y3 - e1);
-            float s0 = (x0 + x1) + (x2 + x3), s1 = (y0 + y1) + (y2 + y3);
-            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-            s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-            s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-            l0 = l0 * al0 + s0;
-            l1 = l1 * al1 + s1;
-            const uint32_t pa[4] = {pack_bf16(x0, x1), pack_bf16(y0, y1), pack_bf16(x2, x3), pack_bf16(y2, y3)};
-            // O += P V: V fragments by transposed 8x8 loads, two 8-wide output tiles per load
-            {
-                const int mi = lane >> 3, ri = lane & 7;
-                const int key = kr + 8 * (mi & 1) + ri;
-#pragma unroll
-                for (int n = 0; n < kNT; n += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vt + sw_off(key, n + (mi >> 1)), b0, b1, b2, b3);
-                    o[n][0] *= al0;
-                    o[n][1] *= al0;
-                    o[n][2] *= al1;
-                    o[n][3] *= al1;
-                    o[n + 1][0] *= al0;
-                    o[n + 1][1] *= al0;
-                    o[n + 1][2] *= al1;
-                    o[n + 1][3] *= al1;
-                    mma16816(o[n], pa, b0, b1);
-                    mma16816(o[n + 1], pa, b2, b3);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(s));
         }
-        // every warp is done with the stages before they are reused for the merge
-        __syncthreads();
-        // this warp's partial: rows g (and g + 8) of (m, l, O)
+    }
+    cp_async_wait<0>();
+    // every warp is done with the stages before they are reused for the merge
+    __syncthreads();
+    {
         float* mw = merge_s + warp * 16 * (D + 2);
         if (t == 0) {
             mw[g * (D + 2) + D] = m0;
@@ -313,7 +312,7 @@ __global__ void __launch_bounds__(kPipeThreads) decode_pipe_kernel(const __grid_
         }
     }
     __syncthreads();
-    // merge the consumer warps and write this split's partial for each query head
+    // merge the warps and write this split's partial for each query head
     for (int e = threadIdx.x; e < G * (D + 2); e += kPipeThreads) {
         const int hg = e / (D + 2), c = e % (D + 2);
         float M = -INFINITY;
@@ -336,7 +335,6 @@ __global__ void __launch_bounds__(kPipeThreads) decode_pipe_kernel(const __grid_
         else
             a.part_ml[pi * 2] = M;
     }
-    if (threadIdx.x == 0 && *abort_flag) set_status(a.status, DMA_ERR_TIMEOUT);
 }
 
 template <int D>
@@ -362,41 +360,11 @@ __global__ void __launch_bounds__(D) decode_pipe_merge_kernel(int nsplit, const 
     if (lse && d == 0) lse[bh] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-bool make_rows_map(CUtensorMap* m, const void* base, int64_t rows, int D)
-{
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_tiled();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
 cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, int Lmax, const int32_t* cache_len,
                          int H, int Hkv, const float* scores, const dma_kept_t* kept, float scale, void* o,
                          float* lse, void* ws, int nsplit, int* status, cudaStream_t st)
 {
-    CUtensorMap km, vm;
-    if (!make_rows_map(&km, Kc, (int64_t)B * Lmax * Hkv, D) || !make_rows_map(&vm, Vc, (int64_t)B * Lmax * Hkv, D))
-        return cudaErrorInvalidValue;
     PipeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.cache_len = cache_len;
@@ -405,7 +373,6 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     a.top_count = kept->top_count;
     a.part_o = static_cast<float*>(ws);
     a.part_ml = a.part_o + (size_t)B * H * nsplit * D;
-    a.status = status;
     a.B = B;
     a.Lmax = Lmax;
     a.H = H;
@@ -418,7 +385,8 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     const int smem = PipeLayout<D>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(decode_pipe_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(km, vm, a);
+    decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(
+        static_cast<const __nv_bfloat16*>(Kc), static_cast<const __nv_bfloat16*>(Vc), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     decode_pipe_merge_kernel<D><<<B * H, D, 0, st>>>(nsplit, a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(o), lse);
     return cudaGetLastError();
