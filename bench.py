@@ -254,8 +254,11 @@ def bench_prefill(args, world, rank, peaks, clocks):
 # ---------------------------------------------------------------- decode ----
 
 def bench_decode(args, world):
+    import dataclasses
     import content_aware_dynamic_dma_b300 as dma
     cfg = wl.WORKLOADS[DECODE_WL]
+    if args.decode_batch != cfg.B:
+        cfg = dataclasses.replace(cfg, B=args.decode_batch)
     B, L, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
     n = args.steps
     nq = args.warmup + n
@@ -302,7 +305,7 @@ def bench_decode(args, world):
     upd_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(n)]
     kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
     gbs = sum(kv_bytes) / (sum(dec_ms) * 1e-3) / 1e9
-    return {"workload": DECODE_WL, "gbs": gbs, "decode_ms": statistics.mean(dec_ms),
+    return {"workload": DECODE_WL if cfg.B == wl.WORKLOADS[DECODE_WL].B else "%s_b%d" % (DECODE_WL, cfg.B), "gbs": gbs, "decode_ms": statistics.mean(dec_ms),
             "score_update_ms": statistics.mean(upd_ms), "step_ms": step_ms,
             "selected_kv_bytes_per_step": statistics.mean(kv_bytes)}
 
@@ -369,6 +372,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode only (a profiling aid: the line then carries no prefill metric)")
+    ap.add_argument("--decode-batch", type=int, default=wl.WORKLOADS[DECODE_WL].B,
+                    help="sequences of the decode workload (smaller values serve profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=4096, help="rows per (b, head) in the CPU-baseline sample")

@@ -43,7 +43,8 @@ struct PipeLayout {
     static constexpr int kBias = kStages * kStage;      // [stage][64] f32
     static constexpr int kMerge = 0;  // [warp][16][D + 2] f32, over the stages once the pipeline is drained
     static_assert(kConsumerWarps * 16 * (D + 2) * 4 <= kBias, "merge area must fit in the stages");
-    static constexpr int kEnd = kBias + kStages * kStageKeys * 4;
+    static constexpr int kJs = kBias + kStages * kStageKeys * 4;  // [kStages + 1][64] key indices
+    static constexpr int kEnd = kJs + (kStages + 1) * kStageKeys * 4;
     static constexpr int kSmemBytes = kEnd + 1024;
 };
 
@@ -149,42 +150,37 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     const __nv_bfloat16* Kh = Kc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
     const __nv_bfloat16* Vh = Vc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
 
-    // copy duty: chunk `part` of rows r0 + kRowsPerPass * m; bias of key threadIdx.x (< 64).
-    // The key indices of a stage are read one stage ahead of its copies, so the copies never
-    // wait for the index loads.
+    // Key indices: thread u < 64 reads the index of key u of a stage one stage before that
+    // stage's copies are issued and leaves it in a small ring in shared memory; the copies
+    // (chunk `part` of rows r0 + kRowsPerPass * m) read their row indices from there.
+    int* js_ring = reinterpret_cast<int*>(sm + L_::kJs);
     const int part = threadIdx.x % kCPR, r0 = threadIdx.x / kCPR;
-    struct StageKeys {
-        int j[kSweeps];
-        int jb;
+    auto key_of = [&](int st) -> int {
+        const int u = u_begin + st * kStageKeys + (int)threadIdx.x;
+        return (st < nst && threadIdx.x < kStageKeys && u < u_end) ? list_key(u, top, n_top, L, a.window) : -1;
     };
-    auto keys_of = [&](int st) {
-        StageKeys k;
-        const int ub = u_begin + st * kStageKeys;
-#pragma unroll
-        for (int m = 0; m < kSweeps; ++m) {
-            const int u = ub + r0 + kRowsPerPass * m;
-            k.j[m] = (st < nst && u < u_end) ? list_key(u, top, n_top, L, a.window) : -1;
-        }
-        const int ubb = ub + (int)threadIdx.x;
-        k.jb = (st < nst && threadIdx.x < kStageKeys && ubb < u_end) ? list_key(ubb, top, n_top, L, a.window) : -1;
-        return k;
+    auto put_key = [&](int st, int j) {
+        if (threadIdx.x < kStageKeys) js_ring[(st % (kStages + 1)) * kStageKeys + threadIdx.x] = j;
     };
-    auto issue = [&](int st, const StageKeys& k) {
+    auto issue = [&](int st) {
         if (st < nst) {
             const int s = st % kStages;
+            const int* jr = js_ring + (st % (kStages + 1)) * kStageKeys;
             const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
 #pragma unroll
             for (int m = 0; m < kSweeps; ++m) {
                 const int r = r0 + kRowsPerPass * m;
-                const bool ok = k.j[m] >= 0;
-                const int64_t off = (int64_t)(ok ? k.j[m] : 0) * row_stride + part * 8;
+                const int j = jr[r];
+                const bool ok = j >= 0;
+                const int64_t off = (int64_t)(ok ? j : 0) * row_stride + part * 8;
                 cp_async16(kt + sw_off(r, part), Kh + off, ok);
                 cp_async16(vt + sw_off(r, part), Vh + off, ok);
             }
             if (threadIdx.x < kStageKeys) {
+                const int j = jr[threadIdx.x];
                 float* bd = bias_s + s * kStageKeys + threadIdx.x;
-                if (k.jb >= 0)
-                    cp_async4(smem_u32(bd), sc + k.jb);
+                if (j >= 0)
+                    cp_async4(smem_u32(bd), sc + j);
                 else
                     *bd = -INFINITY;
             }
@@ -216,26 +212,38 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     const int kr = 16 * warp;  // this warp's 16 keys of each stage
 
 #pragma unroll
-    for (int st = 0; st < kStages - 1; ++st) issue(st, keys_of(st));
-    StageKeys next = keys_of(kStages - 1);
+    for (int st = 0; st < kStages; ++st) put_key(st, key_of(st));
+    __syncthreads();
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) issue(st);
     for (int st = 0; st < nst; ++st) {
+        const int jn = key_of(st + kStages);  // in flight while this stage is computed
         cp_async_wait<kStages - 2>();  // this thread's copies of stage st have landed
         __syncthreads();               // everyone's have; everyone is done with stage st - 1
-        issue(st + kStages - 1, next);  // into the slot of stage st - 1
-        next = keys_of(st + kStages);
+        issue(st + kStages - 1);       // into the slot of stage st - 1
         const int s = st % kStages;
         const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
         // logits: two 8-key tiles
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            // even and odd k-steps in separate accumulators: two short dependency chains
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
             const int mi = lane >> 3, ri = lane & 7;
             const int key = kr + 8 * (mi >> 1) + ri;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t b0, b1, b2, b3;
+            for (int kk = 0; kk < D / 16; kk += 2) {
+                uint32_t b0, b1, b2, b3, e0, e1, e2, e3;
                 ldsm_x4(kt + sw_off(key, 2 * kk + (mi & 1)), b0, b1, b2, b3);
+                ldsm_x4(kt + sw_off(key, 2 * kk + 2 + (mi & 1)), e0, e1, e2, e3);
                 mma16816(c0, qa[kk], b0, b1);
                 mma16816(c1, qa[kk], b2, b3);
+                mma16816(d0, qa[kk + 1], e0, e1);
+                mma16816(d1, qa[kk + 1], e2, e3);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                c0[e] += d0[e];
+                c1[e] += d1[e];
             }
         }
         const float* bs = bias_s + s * kStageKeys + kr;
@@ -291,6 +299,7 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
                 mma16816(o[n + 1], pa, b2, b3);
             }
         }
+        put_key(st + kStages, jn);  // read after the next iteration's barrier
     }
     cp_async_wait<0>();
     // every warp is done with the stages before they are reused for the merge

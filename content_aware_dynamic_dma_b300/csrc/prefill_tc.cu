@@ -351,29 +351,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const __nv_bfloat16* Kh = a.K + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
         const __nv_bfloat16* Vh = a.V + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
         const int64_t kv_stride = (int64_t)a.Hkv * D;
-        uint32_t pend = 0;  // full barrier of the last group issued by this thread, not yet signalled
-        // signals the pending group once it has landed (all: wait for every group of this thread)
-        auto signal_pending = [&](bool all) {
-            if (!pend) return;
-            if (all)
-                cp_async_wait<0>();
-            else
-                cp_async_wait<1>();
-            fence_proxy_async_smem();  // the copies are read by the tensor core (async proxy)
-            mbar_arrive(pend);
-            pend = 0;
-        };
-        // waits for a phase; the pending group is signalled first unless the phase is already there,
-        // so that no consumer waits on this thread while it waits on the consumers
-        auto acquire = [&](int barid, int parity) -> bool {
-            if (!mbar_try_wait(bar(barid), parity)) signal_pending(true);
-            return wait_warp(barid, parity);
-        };
-        auto committed = [&](int barid) {
-            cp_async_commit();
-            signal_pending(false);
-            pend = bar(barid);
-        };
+        // Copies never wait for their own completion: each group ends with an arrival that the
+        // barrier receives once the thread's copies have landed.  The consumer (the MMA thread)
+        // orders them for the tensor core's reads with a proxy fence after its wait.
+        auto acquire = [&](int barid, int parity) -> bool { return wait_warp(barid, parity); };
+        auto committed = [&](int barid) { cp_async_arrive(bar(barid)); };
         auto copy_rows = [&](uint32_t tile, const int* js, const __nv_bfloat16* base) {
 #pragma unroll 4
             for (int m = 0; m < kSweeps; ++m) {
@@ -417,16 +399,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive(bar(kBarIdxEmpty + r));  // done with this slot's indices
                 return true;
             };
+            // V of a block is needed (by PV) before K of the next one (by the next S)
             ok = load_k(t0);
             for (int k = 0; k < nblk && ok; ++k) {
-                if (k + 1 < nblk) ok = load_k(t0 + k + 1);
-                if (ok) ok = load_v(t0 + k);
+                ok = load_v(t0 + k);
+                if (ok && k + 1 < nblk) ok = load_k(t0 + k + 1);
             }
         }
-        if (ok)
-            signal_pending(true);
-        else
-            cp_async_wait<0>();  // the copies already issued land before shared memory goes away
+        cp_async_wait_all();  // the copies already issued land before shared memory goes away
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
         regs_decrease<kRegsControl>();
@@ -455,6 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!(ok = mbar_wait(bar(kBarQFull), p & 1, abort_flag, kWaitNs))) break;
                 const int t0 = p * nblk;
                 if (!(ok = mbar_wait(bar(kBarKFull + (t0 & 1)), (t0 >> 1) & 1, abort_flag, kWaitNs))) break;
+                fence_proxy_async_smem();  // the cp.async writes (generic proxy) before the MMA reads them
                 tc_fence_after();
                 issue_s(0, t0 & 1);
                 mma_commit(bar(kBarSFull + 0));
@@ -468,10 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int t1 = t + 1, s1 = t1 & 1;
                     if (!(ok = mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, kWaitNs))) break;
                     if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, kWaitNs))) break;
+                    fence_proxy_async_smem();
                     tc_fence_after();
                     issue_pv(0, s, k == 0);
                     if (k + 1 < nblk) {
                         if (!(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, kWaitNs))) break;
+                        fence_proxy_async_smem();
                         tc_fence_after();
                         issue_s(0, s1);
                         mma_commit(bar(kBarSFull + 0));

@@ -117,6 +117,15 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The barrier receives one arrival from this thread once every cp.async it has
+// issued so far has landed (the barrier's count must include this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA ----
 
 // Four rows (row coordinates r0..r3, column coordinate col) of a 2-D tensor
