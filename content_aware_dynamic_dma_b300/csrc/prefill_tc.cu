@@ -342,11 +342,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= kCopyWarp0) {
         // -------------------------------------------------------------- copies
         regs_decrease<kRegsControl>();
-        constexpr int kCPR = D / 8;                      // 16-byte chunks per row
-        constexpr int kRowsPerSweep = kCopyThreads / kCPR;
+        constexpr int kPPR = D / 16;                     // 32-byte chunk pairs per row
+        constexpr int kRowsPerSweep = kCopyThreads / kPPR;
         constexpr int kSweeps = kBN / kRowsPerSweep;
         const int ct = threadIdx.x - kCopyWarp0 * 32;
-        const int part = ct % kCPR, r0 = ct / kCPR;
+        const int pair = ct % kPPR, r0 = ct / kPPR;
+        const int part = 2 * pair;  // first of the two 16-byte chunks
         const uint32_t sw_part = (uint32_t)((part >> 3) * L::kHalf);
         const __nv_bfloat16* Kh = a.K + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
         const __nv_bfloat16* Vh = a.V + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
@@ -361,8 +362,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int m = 0; m < kSweeps; ++m) {
                 const int row = r0 + kRowsPerSweep * m;
                 const int j = js[row];
-                const uint32_t dst = tile + sw_part + row * 128 + ((((uint32_t)part & 7u) ^ ((uint32_t)row & 7u)) << 4);
-                cp_async16(dst, base + (int64_t)(j >= 0 ? j : 0) * kv_stride, j >= 0);
+                const uint32_t rb = tile + sw_part + row * 128;
+                const uint32_t x = (uint32_t)row & 7u;
+                const __nv_bfloat16* src = base + (int64_t)(j >= 0 ? j : 0) * kv_stride;
+                cp_async16(rb + (((uint32_t)(part & 7) ^ x) << 4), src, j >= 0);
+                cp_async16(rb + (((uint32_t)((part + 1) & 7) ^ x) << 4), src + 8, j >= 0);
             }
         };
         bool ok = true;
@@ -376,8 +380,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int m = 0; m < kSweeps; ++m) {
                     const int row = r0 + kRowsPerSweep * m;
                     const int i = q0 + row;
-                    const uint32_t dst = tile + sw_part + row * 128 + ((((uint32_t)part & 7u) ^ ((uint32_t)row & 7u)) << 4);
-                    cp_async16(dst, a.Q + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + part * 8, i < a.S);
+                    const uint32_t rb = tile + sw_part + row * 128;
+                    const uint32_t x = (uint32_t)row & 7u;
+                    const __nv_bfloat16* src = a.Q + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + part * 8;
+                    cp_async16(rb + (((uint32_t)(part & 7) ^ x) << 4), src, i < a.S);
+                    cp_async16(rb + (((uint32_t)((part + 1) & 7) ^ x) << 4), src + 8, i < a.S);
                 }
             }
             committed(kBarQFull);
@@ -447,15 +454,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int k = 0; k < nblk; ++k) {
                     const int t = t0 + k, s = t & 1;
                     const int t1 = t + 1, s1 = t1 & 1;
+                    // this block's V and the next block's K (both copied by cp.async), then one
+                    // proxy fence for both: their writes must be ordered before the tensor core's reads
                     if (!(ok = mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, kWaitNs))) break;
-                    if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, kWaitNs))) break;
+                    if (k + 1 < nblk && !(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, kWaitNs)))
+                        break;
                     fence_proxy_async_smem();
+                    if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, kWaitNs))) break;
                     tc_fence_after();
                     issue_pv(0, s, k == 0);
                     if (k + 1 < nblk) {
-                        if (!(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, kWaitNs))) break;
-                        fence_proxy_async_smem();
-                        tc_fence_after();
                         issue_s(0, s1);
                         mma_commit(bar(kBarSFull + 0));
                     } else {
