@@ -46,6 +46,15 @@ DECODE_WL = "decode_b64_l32k_bf16"
 LAUNCHES_SELECT_TOKEN = 19  # 4 x (hist, scan, scatter) + rank + table + prefix + boundary + walk + compact + tiles
 LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merge
 
+# DRAM bytes (read + write) of one prefill attention launch on the 64K workload, from an ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same kernel on the 16K workload
+# (B=2, S=16384: 434,152,704 + 241,636,352 bytes) scaled by the tokens processed (x2).  The
+# captured bytes are the compulsory ones -- Q, K, V read once, O and lse written once -- which
+# grow with the tokens.  Valid only for the kernel source it was taken on: reported as null
+# once that source changes.
+PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 2 * (434152704 + 241636352),
+                   "source_sha256": "6c14020110d429cbb2709f657aa7772a5789ff1999d2186933a812a1da8d38c5"}
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -136,6 +145,19 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ------------------------------------------------------------ kept pairs ----
+
+def prefill_traffic(workload: str):
+    import hashlib
+    src = os.path.join(ROOT, "content_aware_dynamic_dma_b300", "csrc", "prefill_tc.cu")
+    try:
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if workload != PREFILL_TRAFFIC["workload"] or sha != PREFILL_TRAFFIC["source_sha256"]:
+        return None
+    return PREFILL_TRAFFIC["bytes"]
+
 
 def kept_pairs(expiry: torch.Tensor, S: int, window: int, block: int, G: int) -> int:
     """Sum over (b, query head, row i) of |kept set of row i|, from the per-key
@@ -419,7 +441,8 @@ def main():
                      "peak": peak, "unit": "TFLOP/s", "frac": round(pf["attn_tflops"] / peak, 4),
                      "frac_of_sustained": round(pf["attn_tflops"] / peaks["bf16_tflops_sustained"], 4)
                      if peaks.get("bf16_tflops_sustained") else None,
-                     "peak_source": peaks["source"] + " bf16 dense (burst)", "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 dense (burst)", "traffic": prefill_traffic(cfg.name),
+                     "traffic_unit": "bytes per launch (DRAM read + write)",
                      "algorithmic": "4*D flop per kept (query, key) pair, exact pair count from the selection"},
         "kernels_ms": {"score": round(pf["score_ms"], 4), "select": round(pf["select_ms"], 4),
                        "attention": round(pf["attn_ms"], 4)},
