@@ -408,14 +408,28 @@ bool decode_pipe_supported(dma_dtype_t dt, int B, int Lmax, int H, int Hkv, int 
     return dt == DMA_BF16 && (D == 64 || D == 128) && H / Hkv <= 16 && (int64_t)B * Lmax * Hkv < ((int64_t)1 << 31);
 }
 
-// Splits per (sequence, KV head): enough CTAs for about four waves of two per
-// SM, never more than the 64-row chunks of the longest list (the workspace is
-// sized for that many).
+// Splits per (sequence, KV head): among the counts that give at least about four
+// waves of resident CTAs (two per SM), the one whose last wave is fullest -- a
+// grid of 5.2 waves leaves four fifths of the machine idle during its last one.
+// Never more than the 64-row chunks of the longest list (the workspace is sized
+// for that many).
 int decode_pipe_splits(int B, int Hkv, int top_cap, int window)
 {
-    const int max_split = (top_cap + window + 63) / 64;
-    const int want = (4 * 2 * 148 + B * Hkv - 1) / (B * Hkv);
-    return std::max(1, std::min(max_split, want));
+    const int max_split = std::max(1, (top_cap + window + 63) / 64);
+    const int slots = 2 * 148;
+    const int segs = B * Hkv;
+    const int want = std::max(1, (4 * slots + segs - 1) / segs);
+    int best = std::min(max_split, want);
+    double best_eff = 0.0;
+    for (int n = want; n <= std::min(max_split, 3 * want); ++n) {
+        const double waves = (double)segs * n / slots;
+        const double eff = waves / std::ceil(waves);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = n;
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, int B, int Lmax,

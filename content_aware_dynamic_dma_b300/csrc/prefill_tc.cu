@@ -14,15 +14,16 @@
 // One CTA = one (batch, KV head, query tile); it serves all G = H / Hkv query
 // heads of the KV head, two at a time (two "M-tiles" of 128 rows), so each
 // gathered K/V block is fetched once per pair of query heads.  Roles:
-//   warps 0-3 / 4-7  softmax of M-tile A / B: thread = one query row (= one
-//                    tensor-memory lane); S from tensor memory, masked online
-//                    softmax in the log2 domain, P (bf16) written back over S
-//   warp 8           MMA issue (one thread): S = Q K^T (both operands in shared
+//   warps 0-7 / 8-15 softmax of M-tile A / B: a thread takes one half (64
+//                    columns) of one query row (= one tensor-memory lane); S from
+//                    tensor memory, masked online softmax in the log2 domain, P
+//                    (bf16) written back over S
+//   warp 16          MMA issue (one thread): S = Q K^T (both operands in shared
 //                    memory), O += P V (P from tensor memory, V in shared memory)
-//   warp 9           key metadata: runs up to four blocks ahead, filling a ring
+//   warp 17          key metadata: runs up to four blocks ahead, filling a ring
 //                    with each block's key indices, bias (score, log2 units),
 //                    keep intervals and an "every row keeps every key" flag
-//   warps 10-11      copies: Q tiles and the K and V rows of each block,
+//   warps 18-19      copies: Q tiles and the K and V rows of each block,
 //                    gathered with 16-byte cp.async into the 128-byte-swizzled
 //                    operand layout (a TMA tile::gather4 moves only about 8
 //                    bytes per cycle per SM, a quarter of what this needs)
@@ -49,17 +50,18 @@ using namespace tc;
 
 constexpr int kBN = 128;            // keys per block
 constexpr int kRowsPerTile = kQTile;  // 128 query rows per M-tile
-constexpr int kTcThreads = 384;  // three warpgroups
-constexpr int kMmaWarp = 8;
-constexpr int kMetaWarp = 9;
-constexpr int kCopyWarp0 = 10;  // warps 10 and 11
+constexpr int kTcThreads = 640;  // five warpgroups
+constexpr int kSoftmaxWarps = 16;
+constexpr int kMmaWarp = 16;
+constexpr int kMetaWarp = 17;
+constexpr int kCopyWarp0 = 18;  // warps 18 and 19
 constexpr int kCopyThreads = 64;
 constexpr int kIdxStages = 4;   // depth of the key-metadata ring
-// Registers per thread: 168 at launch (384 threads); the third warpgroup (MMA,
-// metadata, copies) gives registers to the two softmax warpgroups:
-// 128 * 88 + 256 * 208 = 384 * 168.
-constexpr int kRegsControl = 88;
-constexpr int kRegsSoftmax = 208;
+// Registers per thread: 96 at launch (640 threads); the fifth warpgroup (MMA,
+// metadata, copies) gives registers to the four softmax warpgroups:
+// 128 * 64 + 512 * 104 = 640 * 96.
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 104;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -96,7 +98,8 @@ struct Layout {
     // then the all-full flag
     static constexpr int kIdx = 6 * kTile;
     static constexpr int kIdxSlot = 5 * kBN * 4 + 16;
-    static constexpr int kFlags = kIdx + kIdxStages * kIdxSlot;  // unused tail, kept for alignment
+    static constexpr int kXch = kIdx + kIdxStages * kIdxSlot;  // [M-tile][slot][half][128] f32
+    static constexpr int kFlags = kXch + 2 * 3 * 2 * kBN * 4;   // unused tail, kept for alignment
     static constexpr int kBars = kFlags + 64;
     static constexpr int kMisc = kBars + 8 * kNumBars;  // tmem base, abort flag
     static constexpr int kEnd = kMisc + 16;
@@ -250,15 +253,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         for (int i = 0; i < kIdxStages; ++i) {
             mbar_init(bar(kBarIdxFull + i), 32);
-            mbar_init(bar(kBarIdxEmpty + i), 8 + 2);  // eight softmax warps and two copy warps
+            mbar_init(bar(kBarIdxEmpty + i), kSoftmaxWarps + 2);  // the softmax warps and two copy warps
         }
         mbar_init(bar(kBarQFull), kCopyThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarKFull + i), kCopyThreads);
             mbar_init(bar(kBarVFull + i), kCopyThreads);
         }
-        mbar_init(bar(kBarPFull + 0), 128);
-        mbar_init(bar(kBarPFull + 1), 128);
+        mbar_init(bar(kBarPFull + 0), 256);
+        mbar_init(bar(kBarPFull + 1), 256);
         mbar_init_fence();
     }
     if (warp == kMmaWarp) tmem_alloc<512>(smem_u32(tmem_slot));
@@ -494,14 +497,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax
+        // Two warpgroups per M-tile: the thread of (row r, half hc) takes columns
+        // [64 hc, 64 hc + 64) of S and P and [D/2 hc, D/2 hc + D/2) of O.  The halves of a
+        // row exchange their block maxima through shared memory (one named barrier per
+        // block), so both take exponents against the same running maximum; each keeps its
+        // own part of the row sum, added up at the end.
         regs_increase<kRegsSoftmax>();
-        const int x = warp >> 2;      // M-tile (warpgroup)
+        constexpr int kHC = kBN / 2;   // S columns per half
+        constexpr int kHD = D / 2;     // O columns per half
+        const int x = warp >> 3;       // M-tile
+        const int hc = (warp >> 2) & 1;  // column half
         const int quarter = warp & 3;  // tensor-memory lane quarter
         const int r = quarter * 32 + lane;
         const int i = q0 + r;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + 256 + 128 * x + lane_off;
-        const uint32_t tO = tmem + 128 * x + lane_off;
+        const uint32_t tS = tmem + 256 + 128 * x + kHC * hc + lane_off;   // this half's S columns
+        const uint32_t tP = tmem + 256 + 128 * x + (kHC / 2) * hc + lane_off;  // this half's P columns
+        const uint32_t tO = tmem + 128 * x + kHD * hc + lane_off;
+        float* xch = reinterpret_cast<float*>(sm + L::kXch) + x * (3 * 2 * kRowsPerTile);  // [slot][half][row]
+        const int col0 = kHC * hc;
         bool ok = true;
         for (int p = 0; p < npass && ok; ++p) {
             const int nm = (2 * p + 1 < a.G) ? 2 : 1;
@@ -515,17 +529,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!(ok = wait_warp(kBarSFull + x, t & 1))) break;
                 tc_fence_after();
                 const int* js = idx_slot(ridx);
-                const float* mb = reinterpret_cast<const float*>(js + kBN);
+                const float* mb = reinterpret_cast<const float*>(js + kBN) + col0;
                 const int all_full = js[5 * kBN];
                 // keep bits of this row for a block that needs a mask (computed before S is held
                 // in registers): kept iff j <= i < j + window  or  lo_j <= i < expiry_j
-                uint32_t kbits[kBN / 32] = {~0u, ~0u, ~0u, ~0u};
+                uint32_t kbits[kHC / 32] = {~0u, ~0u};
                 if (!all_full) {
-                    const int* mj = js + 2 * kBN;
-                    const int* mlo = js + 3 * kBN;
-                    const int* mtl = js + 4 * kBN;
+                    const int* mj = js + 2 * kBN + col0;
+                    const int* mlo = js + 3 * kBN + col0;
+                    const int* mtl = js + 4 * kBN + col0;
 #pragma unroll
-                    for (int w32 = 0; w32 < kBN / 32; ++w32) {
+                    for (int w32 = 0; w32 < kHC / 32; ++w32) {
                         uint32_t bits = 0;
 #pragma unroll
                         for (int cc = 0; cc < 32; cc += 4) {
@@ -541,57 +555,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         kbits[w32] = bits;
                     }
                 }
-                // S row of this thread: four loads in flight, one wait
-                float xv[kBN];
+                // this half of the S row: two loads in flight, one wait
+                float xv[kHC];
                 {
-                    uint32_t r0[32], r1[32], r2[32], r3[32];
+                    uint32_t r0[32], r1[32];
                     tmem_ld32(tS + 0, r0);
                     tmem_ld32(tS + 32, r1);
-                    tmem_ld32(tS + 64, r2);
-                    tmem_ld32(tS + 96, r3);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         xv[e] = __uint_as_float(r0[e]);
                         xv[32 + e] = __uint_as_float(r1[e]);
-                        xv[64 + e] = __uint_as_float(r2[e]);
-                        xv[96 + e] = __uint_as_float(r3[e]);
                     }
                 }
                 // logits in log2 units: x = S * scale * log2(e) + bias * log2(e)
                 const f2 cc2 = mk2(a.c_log2, a.c_log2);
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (all_full) {
 #pragma unroll
-                    for (int c = 0; c < kBN; c += 4) {
-                        const float4 bb = *reinterpret_cast<const float4*>(mb + c);
-                        f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
-                        f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
-                        split2(x01, xv[c], xv[c + 1]);
-                        split2(x23, xv[c + 2], xv[c + 3]);
-                        const int q = (c / 4) & 3;
-                        mx[q] = max3(mx[q], xv[c], xv[c + 1]);
-                        mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN; c += 4) {
-                        const float4 bb = *reinterpret_cast<const float4*>(mb + c);
-                        f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
-                        f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
-                        split2(x01, xv[c], xv[c + 1]);
-                        split2(x23, xv[c + 2], xv[c + 3]);
+                for (int c = 0; c < kHC; c += 4) {
+                    const float4 bb = *reinterpret_cast<const float4*>(mb + c);
+                    f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
+                    f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
+                    split2(x01, xv[c], xv[c + 1]);
+                    split2(x23, xv[c + 2], xv[c + 3]);
+                    if (!all_full) {
                         const uint32_t bits = kbits[c / 32] >> (c % 32);
                         if (!(bits & 1u)) xv[c] = -INFINITY;
                         if (!(bits & 2u)) xv[c + 1] = -INFINITY;
                         if (!(bits & 4u)) xv[c + 2] = -INFINITY;
                         if (!(bits & 8u)) xv[c + 3] = -INFINITY;
-                        const int q = (c / 4) & 3;
-                        mx[q] = max3(mx[q], xv[c], xv[c + 1]);
-                        mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
                     }
+                    const int q = (c / 4) & 3;
+                    mx[q] = max3(mx[q], xv[c], xv[c + 1]);
+                    mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
                 }
-                const float m_blk = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+                // block maximum of the whole row: exchange with the other half
+                float m_blk = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+                {
+                    // (the barrier also orders this half's S loads before the other half's P
+                    // stores, which land in tensor-memory columns that held this half's S)
+                    float* xb = xch + (t & 1) * (2 * kRowsPerTile);
+                    xb[hc * kRowsPerTile + r] = m_blk;
+                    tc_fence_before();
+                    named_bar_sync(1 + x, 256);
+                    tc_fence_after();
+                    m_blk = fmaxf(m_blk, xb[(1 - hc) * kRowsPerTile + r]);
+                }
                 // The maximum of a row moved up: what it has accumulated is rescaled below.
                 const bool raise = m_blk > m_used + kRescaleThreshold;
                 const bool rescale = raise && k > 0 && m_used != -INFINITY;
@@ -601,7 +610,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const f2 me2 = mk2(m_eff, m_eff);
                 f2 ls[4] = {mk2(0.f, 0.f), mk2(0.f, 0.f), mk2(0.f, 0.f), mk2(0.f, 0.f)};
 #pragma unroll
-                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                for (int c0 = 0; c0 < kHC; c0 += 32) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -614,12 +623,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ls[e & 3] = add2(ls[e & 3], mk2(p0, p1));
                         pk[e] = pack_bf16(p0, p1);
                     }
-                    tmem_st16(tS + c0 / 2, pk);
+                    tmem_st16(tP + c0 / 2, pk);
                 }
                 {
-                    const f2 t = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
+                    const f2 tt = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
                     float t0, t1;
-                    split2(t, t0, t1);
+                    split2(tt, t0, t1);
                     l = l * alpha + (t0 + t1);
                 }
                 // O *= alpha for the rows whose maximum moved (tcgen05.ld/st are warp-collective:
@@ -628,25 +637,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (__any_sync(0xffffffffu, rescale)) {
                     const f2 al2 = mk2(alpha, alpha);
 #pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 64) {
-                        uint32_t o0[32], o1[32];
+                    for (int c0 = 0; c0 < kHD; c0 += 32) {
+                        uint32_t o0[32];
                         tmem_ld32(tO + c0, o0);
-                        tmem_ld32(tO + c0 + 32, o1);
                         tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
                             f2 v0 = mul2(mk2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), al2);
-                            f2 v1 = mul2(mk2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), al2);
-                            float y0, y1, y2, y3;
+                            float y0, y1;
                             split2(v0, y0, y1);
-                            split2(v1, y2, y3);
                             o0[e] = __float_as_uint(y0);
                             o0[e + 1] = __float_as_uint(y1);
-                            o1[e] = __float_as_uint(y2);
-                            o1[e + 1] = __float_as_uint(y3);
                         }
                         tmem_st32(tO + c0, o0);
-                        tmem_st32(tO + c0 + 32, o1);
                     }
                 }
                 tmem_st_wait();
@@ -656,13 +659,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive(bar(kBarIdxEmpty + ridx));  // done with this block's metadata
             }
             if (!ok) break;
-            // epilogue: O = accumulator / l
+            // epilogue: O = accumulator / (sum of both halves' row sums)
+            float l_row;
+            {
+                float* xb = xch + 2 * (2 * kRowsPerTile);  // its own slot: the blocks use slots 0 and 1
+                xb[hc * kRowsPerTile + r] = l;
+                named_bar_sync(1 + x, 256);
+                l_row = l + xb[(1 - hc) * kRowsPerTile + r];
+                named_bar_sync(1 + x, 256);  // both halves have read before the slot is reused
+            }
             if (!(ok = wait_warp(kBarOFull + x, p & 1))) break;
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            __nv_bfloat16* op = a.O + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            __nv_bfloat16* op = a.O + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + kHD * hc;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kHD / 32; ++c) {
                 uint32_t rg[32];
                 tmem_ld32(tO + 32 * c, rg);
                 tmem_ld_wait();
@@ -679,8 +690,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (a.lse && i < a.S)
-                a.lse[((int64_t)b * a.H + hq) * a.S + i] = l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+            if (a.lse && hc == 0 && i < a.S)
+                a.lse[((int64_t)b * a.H + hq) * a.S + i] = l_row > 0.f ? (m_used + __log2f(l_row)) * kLn2 : -INFINITY;
             tc_fence_before();
         }
     }

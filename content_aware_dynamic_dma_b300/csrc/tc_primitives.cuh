@@ -65,6 +65,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep until the phase completes or about
+// `hint_ns` nanoseconds pass, instead of returning at once: waiting warps then
+// leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Suspend-time hint of the waits below (a waiting thread is woken when the phase
+// completes; the hint only bounds how long one poll may sleep).
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds (or at once when *abort is already set by another
 // thread of the CTA), sets *abort and returns false.
@@ -73,8 +93,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if ((it & 15u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
@@ -287,6 +307,12 @@ template <int kRegs>
 __device__ __forceinline__ void regs_decrease()
 {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// Barrier among `count` threads (a multiple of 32) using hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
