@@ -499,9 +499,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------- softmax
         // Two warpgroups per M-tile: the thread of (row r, half hc) takes columns
         // [64 hc, 64 hc + 64) of S and P and [D/2 hc, D/2 hc + D/2) of O.  The halves of a
-        // row exchange their block maxima through shared memory (one named barrier per
-        // block), so both take exponents against the same running maximum; each keeps its
-        // own part of the row sum, added up at the end.
+        // row exchange their block maxima through shared memory (one hardware barrier per
+        // block), so both take exponents against the same running maximum; each keeps its own
+        // part of the row sum, added up at the end.
+        // A wait that runs out never makes a thread leave on its own: the 256 threads of an
+        // M-tile carry their verdict to the next exchange, which ANDs it over all of them, and
+        // leave together.  So no thread is ever left at a hardware barrier that its partners
+        // have walked away from.
         regs_increase<kRegsSoftmax>();
         constexpr int kHC = kBN / 2;   // S columns per half
         constexpr int kHD = D / 2;     // O columns per half
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* xch = reinterpret_cast<float*>(sm + L::kXch) + x * (3 * 2 * kRowsPerTile);  // [slot][half][row]
         const int col0 = kHC * hc;
         bool ok = true;
-        for (int p = 0; p < npass && ok; ++p) {
+        for (int p = 0; p < npass; ++p) {  // left only by all 256 threads of the M-tile together
             const int nm = (2 * p + 1 < a.G) ? 2 : 1;
             if (x >= nm) break;
             const int hq = h * a.G + 2 * p + x;
@@ -525,8 +529,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int k = 0; k < nblk; ++k) {
                 const int t = p * nblk + k;
                 const int ridx = t % kIdxStages;
-                if (!(ok = wait_warp(kBarIdxFull + ridx, (t / kIdxStages) & 1))) break;
-                if (!(ok = wait_warp(kBarSFull + x, t & 1))) break;
+                // (after a failed wait the rest of the block runs on stale data: nothing it reads
+                // or writes leaves this CTA's shared and tensor memory, and the exchange below
+                // ends the pass)
+                ok = ok && wait_warp(kBarIdxFull + ridx, (t / kIdxStages) & 1);
+                ok = ok && wait_warp(kBarSFull + x, t & 1);
                 tc_fence_after();
                 const int* js = idx_slot(ridx);
                 const float* mb = reinterpret_cast<const float*>(js + kBN) + col0;
@@ -597,8 +604,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float* xb = xch + (t & 1) * (2 * kRowsPerTile);
                     xb[hc * kRowsPerTile + r] = m_blk;
                     tc_fence_before();
-                    named_bar_sync(1 + x, 256);
+                    ok = named_bar_and(1 + x, 256, ok);  // the same verdict for both halves
                     tc_fence_after();
+                    if (!ok) break;
                     m_blk = fmaxf(m_blk, xb[(1 - hc) * kRowsPerTile + r]);
                 }
                 // The maximum of a row moved up: what it has accumulated is rescaled below.
@@ -668,7 +676,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 l_row = l + xb[(1 - hc) * kRowsPerTile + r];
                 named_bar_sync(1 + x, 256);  // both halves have read before the slot is reused
             }
-            if (!(ok = wait_warp(kBarOFull + x, p & 1))) break;
+            // (on a failed wait the store is skipped and the next pass's first exchange ends
+            // the loop for both halves)
+            if (!(ok = wait_warp(kBarOFull + x, p & 1))) continue;
             tc_fence_after();
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             __nv_bfloat16* op = a.O + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + kHD * hc;
