@@ -56,6 +56,7 @@ constexpr int kMmaWarp = 16;
 constexpr int kMetaWarp = 17;
 constexpr int kCopyWarp0 = 18;  // warps 18 and 19
 constexpr int kCopyThreads = 64;
+constexpr int kCopyChunks = 4;   // 16-byte chunks of a row that one copy thread takes
 constexpr int kIdxStages = 4;   // depth of the key-metadata ring
 // Registers per thread: 96 at launch (640 threads); the fifth warpgroup (MMA,
 // metadata, copies) gives registers to the four softmax warpgroups:
@@ -345,15 +346,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= kCopyWarp0) {
         // -------------------------------------------------------------- copies
         regs_decrease<kRegsControl>();
-        constexpr int kPPR = D / 16;                     // 32-byte chunk pairs per row
-        constexpr int kRowsPerSweep = kCopyThreads / kPPR;
+        // Each thread copies kCPT consecutive 16-byte chunks of a row (one index load and one
+        // address computation per row for all of them); a sweep covers kRowsPerSweep rows, a
+        // multiple of 8, so the swizzle phase (row mod 8) of a thread's rows never changes.
+        constexpr int kCPR = D / 8;  // 16-byte chunks per row
+        constexpr int kCPT = kCopyChunks < kCPR ? kCopyChunks : kCPR;
+        constexpr int kTPR = kCPR / kCPT;  // threads per row
+        constexpr int kRowsPerSweep = kCopyThreads / kTPR;
         constexpr int kSweeps = kBN / kRowsPerSweep;
+        static_assert(kRowsPerSweep % 8 == 0 && kBN % kRowsPerSweep == 0, "copy sweep shape");
         const int ct = threadIdx.x - kCopyWarp0 * 32;
-        const int pair = ct % kPPR, r0 = ct / kPPR;
-        const int part = 2 * pair;  // first of the two 16-byte chunks
-        const uint32_t sw_part = (uint32_t)((part >> 3) * L::kHalf);
-        const __nv_bfloat16* Kh = a.K + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
-        const __nv_bfloat16* Vh = a.V + ((int64_t)b * a.S * a.Hkv + h) * D + part * 8;
+        const int chunk0 = (ct % kTPR) * kCPT, r0 = ct / kTPR;
+        const uint32_t ph = (uint32_t)r0 & 7u;  // swizzle phase of every row this thread copies
+        // shared-memory offset of chunk i of this thread within its row
+        auto chunk_off = [&](int i) -> uint32_t {
+            const int c = chunk0 + i;
+            return (uint32_t)((c >> 3) * L::kHalf) + ((((uint32_t)c & 7u) ^ ph) << 4);
+        };
+        const __nv_bfloat16* Kh = a.K + ((int64_t)b * a.S * a.Hkv + h) * D + chunk0 * 8;
+        const __nv_bfloat16* Vh = a.V + ((int64_t)b * a.S * a.Hkv + h) * D + chunk0 * 8;
         const int64_t kv_stride = (int64_t)a.Hkv * D;
         // Copies never wait for their own completion: each group ends with an arrival that the
         // barrier receives once the thread's copies have landed.  The consumer (the MMA thread)
@@ -365,11 +376,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int m = 0; m < kSweeps; ++m) {
                 const int row = r0 + kRowsPerSweep * m;
                 const int j = js[row];
-                const uint32_t rb = tile + sw_part + row * 128;
-                const uint32_t x = (uint32_t)row & 7u;
+                const uint32_t rb = tile + row * 128;
                 const __nv_bfloat16* src = base + (int64_t)(j >= 0 ? j : 0) * kv_stride;
-                cp_async16(rb + (((uint32_t)(part & 7) ^ x) << 4), src, j >= 0);
-                cp_async16(rb + (((uint32_t)((part + 1) & 7) ^ x) << 4), src + 8, j >= 0);
+#pragma unroll
+                for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * c, j >= 0);
             }
         };
         bool ok = true;
@@ -383,11 +393,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int m = 0; m < kSweeps; ++m) {
                     const int row = r0 + kRowsPerSweep * m;
                     const int i = q0 + row;
-                    const uint32_t rb = tile + sw_part + row * 128;
-                    const uint32_t x = (uint32_t)row & 7u;
-                    const __nv_bfloat16* src = a.Q + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + part * 8;
-                    cp_async16(rb + (((uint32_t)(part & 7) ^ x) << 4), src, i < a.S);
-                    cp_async16(rb + (((uint32_t)((part + 1) & 7) ^ x) << 4), src + 8, i < a.S);
+                    const uint32_t rb = tile + row * 128;
+                    const __nv_bfloat16* src = a.Q + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + chunk0 * 8;
+#pragma unroll
+                    for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * c, i < a.S);
                 }
             }
             committed(kBarQFull);
