@@ -47,13 +47,14 @@ LAUNCHES_SELECT_TOKEN = 19  # 4 x (hist, scan, scatter) + rank + table + prefix 
 LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merge
 
 # DRAM bytes (read + write) of one prefill attention launch on the 64K workload, from an ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same kernel on the 16K workload
-# (B=2, S=16384: 434,152,704 + 241,636,352 bytes) scaled by the tokens processed (x2).  The
-# captured bytes are the compulsory ones -- Q, K, V read once, O and lse written once -- which
-# grow with the tokens.  Valid only for the kernel source it was taken on: reported as null
-# once that source changes.
-PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 2 * (434152704 + 241636352),
-                   "source_sha256": "6c14020110d429cbb2709f657aa7772a5789ff1999d2186933a812a1da8d38c5"}
+# capture of that launch itself (metrics dram__bytes_read.sum and dram__bytes_write.sum only, one
+# pass): 942.96 MB read + 522.88 MB written, as ncu prints them (to 10 kB).  The compulsory bytes
+# are 805 MB read (Q 537 MB, K and V 268 MB) and 545 MB written (O 537 MB, lse 8 MB); the extra
+# 138 MB of reads are gathered K/V rows fetched again after leaving L2, and the writes fall short
+# of the compulsory bytes by what is still dirty in L2 when the kernel ends.  Valid only for the
+# kernel source it was taken on: reported as null once that source changes.
+PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 942960000 + 522880000,
+                   "source_sha256": "7fdf2a34c653f72bf1c4479f5e80b3d50b71665ae5443f0f5a354a3e1c7276ae"}
 
 
 def load_peaks():

@@ -252,6 +252,30 @@ def test_decode_small_bf16_gqa8(dma):
     _check_decode(dma, gen, B, L, H, Hkv, D, w, window, 3)
 
 
+def test_decode_b1_long_list_bf16(dma):
+    """One sequence with a long kept list: 33 splits per (sequence, KV head) (the 64-row chunk limit)."""
+    B, L, H, Hkv, D, w, window = 1, 8192, 8, 2, 128, 2048, 64
+    gen = lambda bs: wl.make_decode(B, L, H, Hkv, D, torch.bfloat16, seed=505, n_queries=2, device="cuda",
+                                    batches=bs)
+    _check_decode(dma, gen, B, L, H, Hkv, D, w, window, 2)
+
+
+def test_decode_b32_split8_bf16(dma):
+    """32 sequences: eight splits per (sequence, KV head)."""
+    B, L, H, Hkv, D, w, window = 32, 4096, 32, 8, 128, 512, 64
+    gen = lambda bs: wl.make_decode(B, L, H, Hkv, D, torch.bfloat16, seed=506, n_queries=2, device="cuda",
+                                    batches=bs)
+    _check_decode(dma, gen, B, L, H, Hkv, D, w, window, 2, sample=[0, 13, 31])
+
+
+def test_decode_b64_short_list_bf16(dma):
+    """Short kept lists (256 rows): as many splits as 64-row chunks, most of them only partly filled."""
+    B, L, H, Hkv, D, w, window = 64, 1024, 32, 8, 128, 192, 64
+    gen = lambda bs: wl.make_decode(B, L, H, Hkv, D, torch.bfloat16, seed=507, n_queries=2, device="cuda",
+                                    batches=bs)
+    _check_decode(dma, gen, B, L, H, Hkv, D, w, window, 2, sample=[0, 40, 63])
+
+
 def test_decode_b64_l32k_bf16(dma):
     """The full decode workload on the GPU; the oracle checks three sampled sequences."""
     cfg = wl.WORKLOADS["decode_b64_l32k_bf16"]
