@@ -48,13 +48,13 @@ LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merg
 
 # DRAM bytes (read + write) of one prefill attention launch on the 64K workload, from an ncu
 # capture of that launch itself (metrics dram__bytes_read.sum and dram__bytes_write.sum only, one
-# pass): 942.96 MB read + 522.88 MB written, as ncu prints them (to 10 kB).  The compulsory bytes
-# are 805 MB read (Q 537 MB, K and V 268 MB) and 545 MB written (O 537 MB, lse 8 MB); the extra
-# 138 MB of reads are gathered K/V rows fetched again after leaving L2, and the writes fall short
-# of the compulsory bytes by what is still dirty in L2 when the kernel ends.  Valid only for the
-# kernel source it was taken on: reported as null once that source changes.
-PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 942960000 + 522880000,
-                   "source_sha256": "7fdf2a34c653f72bf1c4479f5e80b3d50b71665ae5443f0f5a354a3e1c7276ae"}
+# pass): 939,489,280 bytes read + 522,981,632 bytes written.  The compulsory bytes are 805 MB read
+# (Q 537 MB, K and V 268 MB) and 545 MB written (O 537 MB, lse 8 MB); the extra 134 MB of reads
+# are gathered K/V rows fetched again after leaving L2, and the writes fall short of the
+# compulsory bytes by what is still dirty in L2 when the kernel ends.  Valid only for the kernel
+# source it was taken on: reported as null once that source changes.
+PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 939489280 + 522981632,
+                   "source_sha256": "aa33f5941c9a734a06391d252bafd9817379dbe7ac5ef958efdf045c4e7fd89b"}
 
 
 def load_peaks():

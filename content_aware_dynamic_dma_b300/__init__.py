@@ -61,7 +61,7 @@ class KeptT(ctypes.Structure):
 EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_attn_prefill",
             "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_sparse_attn_decode_noalloc",
             "dma_get_device_status", "dma_status_string", "dma_last_error_message", "dma_set_prefill_kernel",
-            "dma_version")
+            "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version")
 
 
 def _load_lib():
@@ -83,12 +83,15 @@ def _load_lib():
         "dma_status_string": [I],
         "dma_last_error_message": [],
         "dma_set_prefill_kernel": [I],
+        "dma_set_wait_limit_ns": [ctypes.c_uint64],
+        "dma_set_fault_injection": [I],
         "dma_version": [],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = I
+    lib.dma_set_wait_limit_ns.restype = ctypes.c_uint64
     lib.dma_status_string.restype = ctypes.c_char_p
     lib.dma_last_error_message.restype = ctypes.c_char_p
     return lib
@@ -255,6 +258,20 @@ def dma_get_device_status(stream=None) -> int:
 def dma_set_prefill_kernel(which: int) -> int:
     """0 = automatic (tensor-core kernel for bf16), 1 = SIMT kernel."""
     return _lib.dma_set_prefill_kernel(which)
+
+
+DMA_FAULT_NONE = 0
+DMA_FAULT_DROP_ARRIVE = 1
+
+
+def dma_set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' bounded waits for later launches (0 = the default); returns the old one."""
+    return _lib.dma_set_wait_limit_ns(ns)
+
+
+def dma_set_fault_injection(mode: int) -> int:
+    """DMA_FAULT_NONE or DMA_FAULT_DROP_ARRIVE (test aid); returns the old mode, -1 if unknown."""
+    return _lib.dma_set_fault_injection(mode)
 
 
 def dma_version() -> int:

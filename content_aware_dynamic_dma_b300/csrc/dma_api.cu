@@ -1,8 +1,10 @@
 // C ABI of libdma: argument validation, error reporting and kernel dispatch.
 // Every entry point checks its arguments completely before it enqueues any
 // work, so an argument error never leaves a partial launch behind.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -23,6 +25,24 @@ int* g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
 int g_prefill_kernel = 0;  // 0 automatic, 1 SIMT
+
+// Wait limit of the kernels' bounded waits and the fault-injection mode, with their
+// defaults from the environment (DMA_TIMEOUT_NS, DMA_FAULT_INJECT) read at load.
+uint64_t env_wait_ns()
+{
+    const char* v = getenv("DMA_TIMEOUT_NS");
+    if (!v || !*v) return kDefaultWaitNs;
+    char* end = nullptr;
+    const unsigned long long n = strtoull(v, &end, 10);
+    return (end && *end == '\0' && n > 0) ? (uint64_t)n : kDefaultWaitNs;
+}
+int env_fault_mode()
+{
+    const char* v = getenv("DMA_FAULT_INJECT");
+    return (v && (strcmp(v, "drop_arrive") == 0 || strcmp(v, "1") == 0)) ? DMA_FAULT_DROP_ARRIVE : DMA_FAULT_NONE;
+}
+std::atomic<uint64_t> g_wait_ns{env_wait_ns()};
+std::atomic<int> g_fault_mode{env_fault_mode()};
 
 dma_status_t fail(dma_status_t s, const char* fmt, ...)
 {
@@ -131,6 +151,17 @@ const char* dma_status_string(dma_status_t s)
 }
 
 const char* dma_last_error_message(void) { return g_msg; }
+
+uint64_t dma_set_wait_limit_ns(uint64_t ns)
+{
+    return g_wait_ns.exchange(ns ? ns : env_wait_ns());
+}
+
+int dma_set_fault_injection(int mode)
+{
+    if (mode != DMA_FAULT_NONE && mode != DMA_FAULT_DROP_ARRIVE) return -1;
+    return g_fault_mode.exchange(mode);
+}
 
 int dma_set_prefill_kernel(int which)
 {
@@ -267,7 +298,8 @@ dma_status_t dma_sparse_attn_prefill(const void* Q, const void* K, const void* V
     if (g_prefill_kernel == 0 && prefill_tc_supported(dt, B, S, H, Hkv, D)) {
         int* status = nullptr;
         if ((s = status_ptr(&status)) != DMA_OK) return s;
-        e = launch_prefill_tc(Q, K, V, B, S, H, Hkv, D, scores, kept, scale, O, lse, status, st);
+        e = launch_prefill_tc(Q, K, V, B, S, H, Hkv, D, scores, kept, scale, O, lse, status, g_wait_ns.load(),
+                              g_fault_mode.load(), st);
     } else {
         e = launch_prefill_simt(Q, K, V, dt, B, S, H, Hkv, D, scores, kept, scale, O, lse, st);
     }

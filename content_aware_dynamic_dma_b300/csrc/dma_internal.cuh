@@ -70,9 +70,14 @@ cudaError_t launch_prefill_simt(const void* Q, const void* K, const void* V, dma
 
 // Tensor-core prefill (bf16, D = 64 or 128).
 bool prefill_tc_supported(dma_dtype_t dt, int B, int S, int H, int Hkv, int D);
+// Default limit of the kernels' bounded waits.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+// wait_ns: limit of every bounded wait in the kernel; fault_mode: DMA_FAULT_NONE or
+// DMA_FAULT_DROP_ARRIVE (CTA 0 withholds one completion signal, for tests of the timeout path)
 cudaError_t launch_prefill_tc(const void* Q, const void* K, const void* V, int B, int S, int H, int Hkv, int D,
                               const float* scores, const dma_kept_t* kept, float scale, void* O, float* lse,
-                              int* status, cudaStream_t st);
+                              int* status, uint64_t wait_ns, int fault_mode, cudaStream_t st);
 
 // Pipelined bf16 decode (TMA row gathers, mma.sync, split-K).
 bool decode_pipe_supported(dma_dtype_t dt, int B, int Lmax, int H, int Hkv, int D);

@@ -63,7 +63,6 @@ constexpr int kIdxStages = 4;   // depth of the key-metadata ring
 // 128 * 64 + 512 * 104 = 640 * 96.
 constexpr int kRegsControl = 64;
 constexpr int kRegsSoftmax = 104;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 0.f;  // rescale whenever the row maximum rises
@@ -198,10 +197,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+// kFaultTest: the wait limit comes from the arguments and the drop-arrive injection is
+// compiled in; the launches of normal use run the kernel without either (fixed 2 s limit).
+template <int D, bool kFaultTest>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_tc_kernel(const TcArgs a)
+    prefill_tc_kernel(const TcArgs a, const uint64_t test_wait_ns, const int test_drop_arrive)
 {
+    // (test_*: used only by the fault-test instantiation: the wait limit, and whether CTA 0
+    // withholds the copy warps' signal for the K rows of its first block)
+    const uint64_t wait_ns = kFaultTest ? test_wait_ns : kDefaultWaitNs;
     using L = Layout<D>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm =
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // A wait whose outcome is the same for every lane of the warp, so that warp-collective
     // instructions after it are never reached by only part of the warp.
     auto wait_warp = [&](int i, int parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, kWaitNs));
+        return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, abort_flag, wait_ns));
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,7 +410,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!acquire(kBarIdxFull + r, (t / kIdxStages) & 1)) return false;
                 if (use >= 1 && !acquire(kBarKEmpty + s, (use - 1) & 1)) return false;
                 copy_rows(sbase + L::kK + s * L::kTile, idx_slot(r), Kh);
-                committed(kBarKFull + s);
+                // (fault injection for tests: the MMA warp's wait for these rows then runs out)
+                if (!(kFaultTest && test_drop_arrive && blockIdx.x == 0 && t == 0)) committed(kBarKFull + s);
                 return true;
             };
             auto load_v = [&](int t) -> bool {
@@ -451,9 +456,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int p = 0; p < npass && ok; ++p) {
                 const int nm = (2 * p + 1 < a.G) ? 2 : 1;
-                if (!(ok = mbar_wait(bar(kBarQFull), p & 1, abort_flag, kWaitNs))) break;
+                if (!(ok = mbar_wait(bar(kBarQFull), p & 1, abort_flag, wait_ns))) break;
                 const int t0 = p * nblk;
-                if (!(ok = mbar_wait(bar(kBarKFull + (t0 & 1)), (t0 >> 1) & 1, abort_flag, kWaitNs))) break;
+                if (!(ok = mbar_wait(bar(kBarKFull + (t0 & 1)), (t0 >> 1) & 1, abort_flag, wait_ns))) break;
                 fence_proxy_async_smem();  // the cp.async writes (generic proxy) before the MMA reads them
                 tc_fence_after();
                 issue_s(0, t0 & 1);
@@ -468,11 +473,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int t1 = t + 1, s1 = t1 & 1;
                     // this block's V and the next block's K (both copied by cp.async), then one
                     // proxy fence for both: their writes must be ordered before the tensor core's reads
-                    if (!(ok = mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, kWaitNs))) break;
-                    if (k + 1 < nblk && !(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, kWaitNs)))
+                    if (!(ok = mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, wait_ns))) break;
+                    if (k + 1 < nblk && !(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, wait_ns)))
                         break;
                     fence_proxy_async_smem();
-                    if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, kWaitNs))) break;
+                    if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, wait_ns))) break;
                     tc_fence_after();
                     issue_pv(0, s, k == 0);
                     if (k + 1 < nblk) {
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         mma_commit(bar(kBarOFull + 0));
                     }
                     if (nm == 2) {
-                        if (!(ok = mbar_wait(bar(kBarPFull + 1), t & 1, abort_flag, kWaitNs))) break;
+                        if (!(ok = mbar_wait(bar(kBarPFull + 1), t & 1, abort_flag, wait_ns))) break;
                         tc_fence_after();
                         issue_pv(1, s, k == 0);
                     }
@@ -501,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // every MMA issued so far has completed before tensor memory is released
             mma_commit(bar(kBarDrain));
-            mbar_wait_drain(bar(kBarDrain), 0, kWaitNs);
+            mbar_wait_drain(bar(kBarDrain), 0, wait_ns);
         }
         __syncwarp();
     } else {
@@ -725,9 +730,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int D>
 cudaError_t launch_typed(const void* Q, const void* K, const void* V, int B, int S, int H, int Hkv,
                          const float* scores, const dma_kept_t* kept, float scale, void* O, float* lse, int* status,
-                         cudaStream_t st)
+                         uint64_t wait_ns, int fault_mode, cudaStream_t st)
 {
     TcArgs a;
+    const int drop_arrive = fault_mode == DMA_FAULT_DROP_ARRIVE ? 1 : 0;
     a.Q = static_cast<const __nv_bfloat16*>(Q);
     a.K = static_cast<const __nv_bfloat16*>(K);
     a.V = static_cast<const __nv_bfloat16*>(V);
@@ -749,10 +755,12 @@ cudaError_t launch_typed(const void* Q, const void* K, const void* V, int B, int
     a.block = kept->block;
     a.c_log2 = scale * kLog2e;
     const int smem = Layout<D>::kSmemBytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const bool fault_test = wait_ns != kDefaultWaitNs || drop_arrive;
+    auto kernel = fault_test ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)kept->n_qt * B * Hkv;
-    prefill_tc_kernel<D><<<(unsigned)grid, kTcThreads, smem, st>>>(a);
+    kernel<<<(unsigned)grid, kTcThreads, smem, st>>>(a, wait_ns, drop_arrive);
     return cudaGetLastError();
 }
 
@@ -769,10 +777,11 @@ bool prefill_tc_supported(dma_dtype_t dt, int B, int S, int H, int Hkv, int D)
 
 cudaError_t launch_prefill_tc(const void* Q, const void* K, const void* V, int B, int S, int H, int Hkv, int D,
                               const float* scores, const dma_kept_t* kept, float scale, void* O, float* lse,
-                              int* status, cudaStream_t st)
+                              int* status, uint64_t wait_ns, int fault_mode, cudaStream_t st)
 {
-    if (D == 128) return launch_typed<128>(Q, K, V, B, S, H, Hkv, scores, kept, scale, O, lse, status, st);
-    return launch_typed<64>(Q, K, V, B, S, H, Hkv, scores, kept, scale, O, lse, status, st);
+    if (D == 128)
+        return launch_typed<128>(Q, K, V, B, S, H, Hkv, scores, kept, scale, O, lse, status, wait_ns, fault_mode, st);
+    return launch_typed<64>(Q, K, V, B, S, H, Hkv, scores, kept, scale, O, lse, status, wait_ns, fault_mode, st);
 }
 
 }  // namespace dma

@@ -224,6 +224,29 @@ const char* dma_last_error_message(void);
  * available), 1 = SIMT kernel always.  Process-wide; returns the old value. */
 int dma_set_prefill_kernel(int which);
 
+/* Fault detection (a test aid; no effect on results when left at the defaults).
+ * Every wait inside the tensor-core prefill kernel (on an mbarrier that a
+ * copy, the tensor core or another warp completes) gives up after a time
+ * limit: the kernel then records DMA_ERR_TIMEOUT in the device status word
+ * (read by dma_get_device_status), every warp of the CTA leaves its loop, the
+ * copies and tensor-core work already in flight land, and the kernel ends; the
+ * CUDA context stays usable and O holds unspecified values for that launch.
+ *
+ * dma_set_wait_limit_ns: the limit in nanoseconds for launches made after the
+ *   call (process-wide); 0 restores the default, which is DMA_TIMEOUT_NS from
+ *   the environment when the library loads, else 2 s.  Returns the previous
+ *   limit.
+ * dma_set_fault_injection: DMA_FAULT_NONE, or DMA_FAULT_DROP_ARRIVE: in the
+ *   prefill launches that follow, CTA 0 of the tensor-core kernel withholds the
+ *   copy warps' completion signal for the K rows of its first key block, so the
+ *   MMA warp's wait for them runs out (one bounded timeout, then the path
+ *   above).  The default is DMA_FAULT_INJECT=drop_arrive in the environment
+ *   when the library loads, else none.  Returns the previous mode, or -1 (and
+ *   changes nothing) for an unknown mode. */
+enum { DMA_FAULT_NONE = 0, DMA_FAULT_DROP_ARRIVE = 1 };
+uint64_t dma_set_wait_limit_ns(uint64_t ns);
+int dma_set_fault_injection(int mode);
+
 int dma_version(void);
 
 #ifdef __cplusplus

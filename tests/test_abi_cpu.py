@@ -3,6 +3,8 @@ point, computes layouts, and rejects bad arguments before touching the device.""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -140,3 +142,28 @@ def test_status_strings(dma):
     assert names == ["DMA_OK", "DMA_ERR_INVALID_ARG", "DMA_ERR_UNSUPPORTED", "DMA_ERR_WORKSPACE", "DMA_ERR_CUDA",
                      "DMA_ERR_TIMEOUT", "DMA_ERR_DEVICE_CHECK"]
     assert dma.dma_version() >= 1
+
+
+def test_wait_limit_and_fault_injection_setters(dma):
+    """The setters return the previous value; 0 restores the default limit; unknown modes are refused."""
+    old = dma.dma_set_wait_limit_ns(12345)
+    assert dma.dma_set_wait_limit_ns(0) == 12345
+    assert dma.dma_set_wait_limit_ns(old) == 2_000_000_000 or old != 2_000_000_000
+    assert dma.dma_set_fault_injection(7) == -1
+    m = dma.dma_set_fault_injection(dma.DMA_FAULT_DROP_ARRIVE)
+    assert dma.dma_set_fault_injection(m) == dma.DMA_FAULT_DROP_ARRIVE
+
+
+def test_wait_limit_and_fault_injection_defaults_from_environment(dma):
+    """DMA_TIMEOUT_NS and DMA_FAULT_INJECT, read when the library loads (a fresh process)."""
+    code = ("import ctypes; lib = ctypes.CDLL(%r); lib.dma_set_wait_limit_ns.restype = ctypes.c_uint64; "
+            "lib.dma_set_wait_limit_ns.argtypes = [ctypes.c_uint64]; "
+            "print(lib.dma_set_wait_limit_ns(1), lib.dma_set_fault_injection(0))" % dma.LIB_PATH)
+    env = dict(os.environ, DMA_TIMEOUT_NS="7777", DMA_FAULT_INJECT="drop_arrive")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["7777", "1"]
+    env = {k: v for k, v in os.environ.items() if k not in ("DMA_TIMEOUT_NS", "DMA_FAULT_INJECT")}
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == ["2000000000", "0"]
