@@ -171,6 +171,40 @@ def test_masked_keys_are_never_read(dma):
     assert not torch.equal(O1[:, :r0], O2[:, :r0])  # the window did see the changed rows
 
 
+def test_block_mode_full_budget_is_dense_causal(dma):
+    """64-key blocks with a budget of every block and a 64-key window keep all of 0..i for
+    every row: the GPU path against the oracle's dense causal attention with key bias."""
+    S = 1000
+    inp = wl.make_prefill(1, S, 8, 2, 128, torch.bfloat16, seed=801, w_std=0.3)
+    O, lse, scores, kept = gpu_prefill(dma, inp, S, 64, block=64)
+    sc = oracle.score(inp["V"], inp["W"], inp["A"])
+    ex = oracle.select(sc, S, 64)
+    rows = list(range(0, S, 7)) + [S - 1]
+    O_ref, lse_ref = oracle.attend_rows(inp["Q"], inp["K"], inp["V"], sc, ex, rows, 64, 64)
+    dense_ref, dense_lse = oracle.attend_rows(inp["Q"], inp["K"], inp["V"], sc,
+                                              torch.full_like(ex, S + 1), rows, S, 1)
+    assert torch.allclose(O_ref, dense_ref, atol=1e-12, rtol=0)
+    parity.check_outputs(O, dense_ref, lse, dense_lse, rows, torch.bfloat16, 8, 2)
+
+
+def test_per_head_masks_on_the_gpu(dma):
+    """Changing the weights of KV head 1 leaves KV head 0's kept sets and the outputs of its
+    query heads bit-identical on the GPU path, and changes head 1's."""
+    B, S, H, Hkv, D, w, window = 1, 2000, 8, 2, 128, 256, 32
+    inp = wl.make_prefill(B, S, H, Hkv, D, torch.bfloat16, seed=802, w_std=0.3)
+    O, lse, scores, kept = gpu_prefill(dma, inp, w, window)
+    inp2 = dict(inp)
+    W2 = inp["W"].clone()
+    W2[1] = -W2[1]
+    inp2["W"] = W2
+    O2, lse2, scores2, kept2 = gpu_prefill(dma, inp2, w, window)
+    assert torch.equal(kept2.expiry[:, 0], kept.expiry[:, 0])
+    assert not torch.equal(kept2.expiry[:, 1], kept.expiry[:, 1])
+    G = H // Hkv
+    assert torch.equal(O2[:, :, :G], O[:, :, :G]) and torch.equal(lse2[:, :G], lse[:, :G])
+    assert not torch.equal(O2[:, :, G:], O[:, :, G:])
+
+
 def test_simt_and_default_kernels_agree(dma):
     cfg = wl.WORKLOADS["prefill_s4k_gqa_bf16"]
     inp = wl.make_workload(cfg)

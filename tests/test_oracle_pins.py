@@ -294,6 +294,34 @@ def test_attention_window_only_is_sliding_window(oracle_mod):
     assert torch.allclose(lse, ref_lse, atol=1e-12, rtol=0)
 
 
+def test_attention_block_mode_full_budget_with_window_is_dense_causal(oracle_mod):
+    """64-key blocks, a budget of every block and a window >= 64: each row keeps every complete
+    past block plus its own (incomplete) block through the window, i.e. all of 0..i: causal
+    attention with the score as an additive key bias."""
+    S = 150
+    inp = wl.make_prefill(1, S, 4, 2, 64, torch.float32, seed=24, w_std=0.5)
+    O, lse, sc, ex = oracle_mod.prefill(inp["Q"], inp["K"], inp["V"], inp["W"], None, w=S, window=64, block=64)
+    causal = torch.tril(torch.ones(S, S, dtype=torch.bool)).expand(1, 2, S, S)
+    ref, ref_lse = _sdpa_masked(inp["Q"], inp["K"], inp["V"], _bias_mask(sc, causal), 1 / 8.0)
+    assert torch.allclose(O, ref, atol=1e-12, rtol=0)
+    assert torch.allclose(lse, ref_lse, atol=1e-12, rtol=0)
+
+
+def test_per_head_masks_depend_only_on_their_own_weights(oracle_mod):
+    """Each KV head's kept sets and outputs follow its own weights w_h: changing w_1 changes
+    head 1's kept sets and leaves head 0's sets and its query heads' outputs bit-identical."""
+    S, w, win = 64, 12, 3
+    inp = wl.make_prefill(1, S, 4, 2, 64, torch.float32, seed=25, w_std=1.0)
+    O, lse, sc, ex = oracle_mod.prefill(inp["Q"], inp["K"], inp["V"], inp["W"], None, w=w, window=win)
+    W2 = inp["W"].clone()
+    W2[1] = -W2[1] + 0.3
+    O2, lse2, sc2, ex2 = oracle_mod.prefill(inp["Q"], inp["K"], inp["V"], W2, None, w=w, window=win)
+    assert torch.equal(ex2[:, 0], ex[:, 0])
+    assert not torch.equal(ex2[:, 1], ex[:, 1])
+    assert torch.equal(O2[:, :, :2], O[:, :, :2]) and torch.equal(lse2[:, :2], lse[:, :2])
+    assert not torch.equal(O2[:, :, 2:], O[:, :, 2:])
+
+
 @pytest.mark.parametrize("w,window", [(5, 0), (9, 4), (3, 20)])
 def test_attention_general_against_sdpa_with_sorted_sets(oracle_mod, w, window):
     """Top-w (by Python's sort) united with the window, as an SDPA float mask."""
