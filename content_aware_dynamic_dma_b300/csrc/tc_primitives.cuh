@@ -1,17 +1,17 @@
 // Blackwell (sm_103a) building blocks written as inline PTX: mbarriers with
-// bounded waits, TMA row gathers (tile::gather4), tcgen05 tensor-memory
-// allocation, MMA issue and commit, and tensor-memory loads and stores.
+// bounded waits, cp.async copies that complete on an mbarrier, tcgen05
+// tensor-memory allocation, MMA issue and commit, tensor-memory loads and
+// stores, register reallocation and hardware barriers.
 //
 // Shared-memory operand layout used with these helpers (bf16, "SW128"): a tile
 // of R rows x 64 elements is R consecutive 128-byte rows; inside each group of 8
 // rows (1024 bytes) the 16-byte chunk c of row r sits at chunk position
-// c ^ (r & 7).  A TMA load with 128-byte swizzle writes exactly this pattern
-// (computed from the destination address), and the tcgen05 shared-memory
-// descriptor with swizzle mode 128B reads it.  Tiles start on 1024-byte
-// boundaries.
+// c ^ (r & 7).  The copies write this pattern (a TMA load with 128-byte swizzle
+// would write the same one, computed from the destination address), and the
+// tcgen05 shared-memory descriptor with swizzle mode 128B reads it.  Tiles
+// start on 1024-byte boundaries.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -45,11 +45,6 @@ __device__ __forceinline__ void mbar_init_fence()
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
@@ -144,27 +139,6 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// ------------------------------------------------------------------ TMA ----
-
-// Four rows (row coordinates r0..r3, column coordinate col) of a 2-D tensor
-// map with a one-row box, written as four consecutive box rows at dst.  A row
-// coordinate outside the tensor is filled with zeros.  Completion is counted
-// in bytes on `bar`.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2,
-                                            int r3, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
-{
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // ------------------------------------------------------------- tcgen05 -----
@@ -271,16 +245,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-
-// 32 lanes x 16 columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
