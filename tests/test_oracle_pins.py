@@ -9,6 +9,8 @@ head attends to at most k historical positions at every time step).
 """
 import itertools
 import math
+import os
+from fractions import Fraction
 
 import mpmath
 import numpy as np
@@ -424,3 +426,34 @@ def test_select_ranks_at_fp32_precision(oracle_mod):
     assert oracle_mod.top_set(ex, 1) == {0}
     assert oracle_mod.top_set(ex, 3) == {0}
     assert oracle_mod.top_set(ex, 5) == {5}
+
+
+def _golden(name):
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+    V, O = {}, {}
+    for line in open(path):
+        f = line.split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "V":
+            V[int(f[1])] = [float(Fraction(x)) for x in f[2:4]]
+        elif f[0] == "O":
+            O[int(f[1])] = ([float(Fraction(x)) for x in f[2:4]], int(f[4]))
+    return V, O
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_golden_equal_scores_uniform_weights(oracle_mod, mode):
+    """The hand-derived example in tests/golden/equal_scores_uniform_weights.txt."""
+    V, O = _golden("equal_scores_uniform_weights.txt")
+    S = len(V)
+    v = torch.tensor([V[j] for j in range(S)], dtype=torch.float64).view(1, S, 1, 2)
+    q = torch.randn(1, S, 1, 2, dtype=torch.float64, generator=torch.Generator().manual_seed(5))
+    k = torch.zeros(1, S, 1, 2, dtype=torch.float64)
+    W = torch.zeros(1, 2, dtype=torch.float64)
+    out, lse, sc, ex = oracle_mod.prefill(q, k, v, W, None, w=2, window=1, mode=mode)
+    assert torch.allclose(sc, torch.full_like(sc, math.log(2.0)), atol=1e-15, rtol=0)
+    for i in range(S):
+        want, n = O[i]
+        assert torch.allclose(out[0, i, 0], torch.tensor(want, dtype=torch.float64), atol=1e-12, rtol=0), i
+        assert abs(float(lse[0, 0, i]) - (math.log(2.0) + math.log(n))) < 1e-12, i
