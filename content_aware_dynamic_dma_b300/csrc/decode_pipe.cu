@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     float* merge_s = reinterpret_cast<float*>(sm + L_::kMerge);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The merge kernel may be scheduled once every CTA of this grid has started; it waits for
+    // this grid's completion (and its memory) before reading the partials.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int seg = blockIdx.y, split = blockIdx.x;
     const int b = seg / a.Hkv, h = seg % a.Hkv;
     const int G = a.G;
@@ -351,6 +354,9 @@ __global__ void __launch_bounds__(D) decode_pipe_merge_kernel(int nsplit, const 
                                                               const float* __restrict__ part_ml,
                                                               __nv_bfloat16* __restrict__ o, float* __restrict__ lse)
 {
+    // launched as a programmatic dependent of the partial kernel: wait until that grid has
+    // completed and its writes are visible (returns at once without such a dependency)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int bh = blockIdx.x, d = threadIdx.x;
     const float* ml = part_ml + (int64_t)bh * nsplit * 2;
     float M = -INFINITY;
@@ -397,8 +403,20 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(
         static_cast<const __nv_bfloat16*>(Kc), static_cast<const __nv_bfloat16*>(Vc), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_pipe_merge_kernel<D><<<B * H, D, 0, st>>>(nsplit, a.part_o, a.part_ml, static_cast<__nv_bfloat16*>(o), lse);
-    return cudaGetLastError();
+    // the merge launches while the partial kernel's last wave runs (programmatic dependent
+    // launch), so the gap between the two kernels is hidden
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B * H);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_pipe_merge_kernel<D>, nsplit, static_cast<const float*>(a.part_o),
+                              static_cast<const float*>(a.part_ml), static_cast<__nv_bfloat16*>(o), lse);
 }
 
 }  // namespace
