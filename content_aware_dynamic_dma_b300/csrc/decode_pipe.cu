@@ -127,8 +127,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     constexpr int kRowsPerPass = kPipeThreads / kCPR;  // rows covered by one sweep of the CTA
     constexpr int kSweeps = kStageKeys / kRowsPerPass;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, by pointer arithmetic so that accesses through it stay ld/st.shared
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     float* bias_s = reinterpret_cast<float*>(sm + L_::kBias);
     float* merge_s = reinterpret_cast<float*>(sm + L_::kMerge);

@@ -13,17 +13,21 @@
 //
 // One CTA = one (batch, KV head, query tile); it serves all G = H / Hkv query
 // heads of the KV head, two at a time (two "M-tiles" of 128 rows), so each
-// gathered K/V block is fetched once per pair of query heads.  Roles:
-//   warps 0-7 / 8-15 softmax of M-tile A / B: a thread takes one half (64
-//                    columns) of one query row (= one tensor-memory lane); S from
-//                    tensor memory, masked online softmax in the log2 domain, P
-//                    (bf16) written back over S
-//   warp 16          MMA issue (one thread): S = Q K^T (both operands in shared
+// gathered K/V block is fetched once per pair of query heads.  Roles (512
+// threads, four warpgroups):
+//   warps 0-3 / 4-7  softmax of M-tile A / B: a thread owns one query row (= one
+//                    tensor-memory lane): S from tensor memory, masked online
+//                    softmax in the log2 domain, P (bf16) written back over S
+//   warps 8-11       correction: rescales a row's O accumulator in tensor memory
+//                    when its running maximum rises (while the softmax computes
+//                    the exponentials), and writes O / row sum and lse at the end
+//                    of a pass
+//   warp 12          MMA issue (one thread): S = Q K^T (both operands in shared
 //                    memory), O += P V (P from tensor memory, V in shared memory)
-//   warp 17          key metadata: runs up to four blocks ahead, filling a ring
+//   warp 13          key metadata: runs up to four blocks ahead, filling a ring
 //                    with each block's key indices, bias (score, log2 units),
 //                    keep intervals and an "every row keeps every key" flag
-//   warps 18-19      copies: Q tiles and the K and V rows of each block,
+//   warps 14-15      copies: Q tiles and the K and V rows of each block,
 //                    gathered with 16-byte cp.async into the 128-byte-swizzled
 //                    operand layout (a TMA tile::gather4 moves only about 8
 //                    bytes per cycle per SM, a quarter of what this needs)
@@ -48,42 +52,46 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBN = 128;            // keys per block
+constexpr int kBN = 128;              // keys per block
 constexpr int kRowsPerTile = kQTile;  // 128 query rows per M-tile
-constexpr int kTcThreads = 640;  // five warpgroups
-constexpr int kSoftmaxWarps = 16;
-constexpr int kMmaWarp = 16;
-constexpr int kMetaWarp = 17;
-constexpr int kCopyWarp0 = 18;  // warps 18 and 19
+constexpr int kTcThreads = 512;       // four warpgroups
+constexpr int kCorrWarp0 = 8;         // warps 8-11
+constexpr int kMmaWarp = 12;
+constexpr int kMetaWarp = 13;
+constexpr int kCopyWarp0 = 14;  // warps 14 and 15
+constexpr int kSoftmaxWarps = 8;
 constexpr int kCopyThreads = 64;
-constexpr int kCopyChunks = 4;   // 16-byte chunks of a row that one copy thread takes
+constexpr int kCopyChunks = 4;  // 16-byte chunks of a row that one copy thread takes
 constexpr int kIdxStages = 4;   // depth of the key-metadata ring
-// Registers per thread: 96 at launch (640 threads); the fifth warpgroup (MMA,
-// metadata, copies) gives registers to the four softmax warpgroups:
-// 128 * 64 + 512 * 104 = 640 * 96.
+// Registers per thread: 128 at launch (512 threads x 128 = the whole register
+// file); the correction and control warpgroups give registers to the two softmax
+// warpgroups: 256 * 192 + 128 * 64 + 128 * 64 = 512 * 128.
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsCorr = 64;
 constexpr int kRegsControl = 64;
-constexpr int kRegsSoftmax = 104;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsCorr + 128 * kRegsControl <= kTcThreads * 128,
+              "register split exceeds the launch's registers");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 0.f;  // rescale whenever the row maximum rises
-// One exponential pair in kPolyEvery is computed by ex2_poly (0: none).
-constexpr int kPolyEvery = 0;
 
 // barrier slots
 enum : int {
     kBarQFull = 0,
     kBarQEmpty = 1,
-    kBarKFull = 2,     // 2 stages
-    kBarKEmpty = 4,    // 2 stages
-    kBarVFull = 6,     // 2 stages
-    kBarVEmpty = 8,    // 2 stages
-    kBarSFull = 10,    // per M-tile
-    kBarPFull = 12,    // per M-tile
-    kBarOFull = 14,    // per M-tile
+    kBarKFull = 2,    // 2 stages
+    kBarKEmpty = 4,   // 2 stages
+    kBarVFull = 6,    // 2 stages
+    kBarVEmpty = 8,   // 2 stages
+    kBarSFull = 10,   // per M-tile: S of a block is in tensor memory
+    kBarPFull = 12,   // per M-tile: P of a block is in tensor memory
+    kBarOFull = 14,   // per M-tile: the last PV of a pass has completed
     kBarDrain = 16,
-    kBarIdxFull = 17,  // kIdxStages slots
-    kBarIdxEmpty = 17 + kIdxStages,
-    kNumBars = 17 + 2 * kIdxStages
+    kBarAFull = 17,   // per M-tile: the rescale factors of a block are in shared memory
+    kBarOReady = 19,  // per M-tile: O is rescaled for a block (or drained, for a pass's first block)
+    kBarStats = 21,   // per (M-tile, pass parity): the row sums of a pass are in shared memory
+    kBarIdxFull = 25,  // kIdxStages slots
+    kBarIdxEmpty = 25 + kIdxStages,
+    kNumBars = 25 + 2 * kIdxStages
 };
 
 template <int D>
@@ -98,9 +106,9 @@ struct Layout {
     // then the all-full flag
     static constexpr int kIdx = 6 * kTile;
     static constexpr int kIdxSlot = 5 * kBN * 4 + 16;
-    static constexpr int kXch = kIdx + kIdxStages * kIdxSlot;  // [M-tile][slot][half][128] f32
-    static constexpr int kFlags = kXch + 2 * 3 * 2 * kBN * 4;   // unused tail, kept for alignment
-    static constexpr int kBars = kFlags + 64;
+    static constexpr int kAlpha = kIdx + kIdxStages * kIdxSlot;    // [M-tile][row] f32
+    static constexpr int kStats = kAlpha + 2 * kRowsPerTile * 4;   // [parity][M-tile][row] f32 row sums
+    static constexpr int kBars = kStats + 2 * 2 * kRowsPerTile * 4;
     static constexpr int kMisc = kBars + 8 * kNumBars;  // tmem base, abort flag
     static constexpr int kEnd = kMisc + 16;
     static constexpr int kSmemBytes = kEnd + 1024;  // slack for 1024-byte alignment
@@ -126,24 +134,6 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for x <= 8 (x may be -inf): Cody-Waite range reduction
-// x = j + f with j = round(x) and f in [-1/2, 1/2] (the integer j is read out of
-// the mantissa of x + 1.5 * 2^23), then a degree-3 polynomial for 2^f whose
-// coefficients minimise the relative error on [-1/2, 1/2] (about 7.5e-5, far
-// below the bf16 rounding of P), and j is added to the exponent bits.  Results
-// below 2^-126 come out as tiny or zero values.
-__device__ __forceinline__ float ex2_poly(float x)
-{
-    x = fmaxf(x, -126.f);
-    const float t = x + 12582912.f;  // 1.5 * 2^23: round to an integer in the low mantissa bits
-    const float j = t - 12582912.f;
-    const float f = x - j;
-    float p = fmaf(0.0551711433f, f, 0.242609963f);
-    p = fmaf(p, f, 0.693260968f);
-    p = fmaf(p, f, 0.999928117f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 // Packed pairs of fp32 (one instruction for two lanes of arithmetic).
@@ -197,6 +187,60 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The CTA's work unit: (batch, KV head) segment and query tile, and the tile's key list
+// (gathered keys, then the window band).  Every role computes it for itself, from a block
+// index read afresh, so that none of it stays live across the role branches (the roles run
+// with different register budgets).
+struct Geom {
+    int b, h, seg, q0, q1, W, n_g, band_lo, n_all, nblk, npass;
+    const int32_t* gl;
+
+    // key at position u of the tile's list; -1 past the end (and for an out-of-range gathered
+    // index, which is recorded as DMA_ERR_DEVICE_CHECK)
+    __device__ __forceinline__ int key_at(int u, int S, int* status) const
+    {
+        int j = -1;
+        if (u < n_g) {
+            j = gl[u];
+            if (j < 0 || j >= S) {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+                j = -1;
+            }
+        } else if (u < n_all) {
+            j = band_lo + (u - n_g);
+        }
+        return j;
+    }
+};
+
+__device__ __forceinline__ int fresh_ctaid()
+{
+    int v;
+    asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(v));
+    return v;
+}
+
+__device__ __forceinline__ Geom tile_geom(const TcArgs& a, int unit)
+{
+    Geom g;
+    const int nseg = a.B * a.Hkv;
+    const int tile = a.n_qt - 1 - unit / nseg;  // longest tiles first
+    g.seg = unit % nseg;
+    g.b = g.seg / a.Hkv;
+    g.h = g.seg % a.Hkv;
+    g.q0 = tile * kRowsPerTile;
+    g.q1 = min(a.S, g.q0 + kRowsPerTile) - 1;
+    g.W = a.window;
+    g.n_g = min(max(a.tile_cnt[(int64_t)g.seg * a.n_qt + tile], 0), a.tile_stride);
+    g.gl = a.tile_idx + ((int64_t)g.seg * a.n_qt + tile) * a.tile_stride;
+    g.band_lo = g.W > 0 ? max(0, g.q0 - g.W + 1) : g.q1 + 1;
+    const int n_b = g.W > 0 ? g.q1 + 1 - g.band_lo : 0;
+    g.n_all = g.n_g + n_b;
+    g.nblk = (g.n_all + kBN - 1) / kBN;
+    g.npass = (a.G + 1) / 2;
+    return g;
+}
+
 // kFaultTest: the wait limit comes from the arguments and the drop-arrive injection is
 // compiled in; the launches of normal use run the kernel without either (fixed 2 s limit).
 template <int D, bool kFaultTest>
@@ -208,12 +252,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t wait_ns = kFaultTest ? test_wait_ns : kDefaultWaitNs;
     using L = Layout<D>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm =
-        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic so that the compiler keeps every access
+    // through it in the shared state space (ld/st.shared, not generic loads)
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     auto idx_slot = [&](int r) { return reinterpret_cast<int*>(sm + L::kIdx + r * L::kIdxSlot); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kMisc + 4);
+    float* alpha_sm = reinterpret_cast<float*>(sm + L::kAlpha);
+    float* stats_sm = reinterpret_cast<float*>(sm + L::kStats);
     auto bar = [&](int i) { return sbase + L::kBars + 8 * i; };
     // A wait whose outcome is the same for every lane of the warp, so that warp-collective
     // instructions after it are never reached by only part of the warp.
@@ -222,35 +269,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nseg = a.B * a.Hkv;
-    const int unit = blockIdx.x;
-    const int tile = a.n_qt - 1 - unit / nseg;  // longest tiles first
-    const int seg = unit % nseg;
-    const int b = seg / a.Hkv, h = seg % a.Hkv;
-    const int q0 = tile * kRowsPerTile;
-    const int q1 = min(a.S, q0 + kRowsPerTile) - 1;
-    const int W = a.window;
-
-    int n_g = a.tile_cnt[(int64_t)seg * a.n_qt + tile];
-    n_g = min(max(n_g, 0), a.tile_stride);
-    const int32_t* gl = a.tile_idx + ((int64_t)seg * a.n_qt + tile) * a.tile_stride;
-    const int band_lo = W > 0 ? max(0, q0 - W + 1) : q1 + 1;
-    const int n_b = W > 0 ? q1 + 1 - band_lo : 0;
-    const int n_all = n_g + n_b;
-    const int nblk = (n_all + kBN - 1) / kBN;
-    const int npass = (a.G + 1) / 2;
-
-    if (nblk == 0) {
-        // nothing kept for any row of the tile: O = 0, lse = -inf
-        for (int t = threadIdx.x; t < kRowsPerTile * a.G; t += kTcThreads) {
-            const int r = t % kRowsPerTile, g = t / kRowsPerTile, i = q0 + r;
-            if (i > q1) continue;
-            const int hq = h * a.G + g;
-            uint4* op = reinterpret_cast<uint4*>(a.O + (((int64_t)b * a.S + i) * a.H + hq) * D);
-            for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0, 0, 0, 0);
-            if (a.lse) a.lse[((int64_t)b * a.H + hq) * a.S + i] = -INFINITY;
+    {
+        const Geom g = tile_geom(a, blockIdx.x);
+        if (g.nblk == 0) {
+            // nothing kept for any row of the tile: O = 0, lse = -inf
+            for (int t = threadIdx.x; t < kRowsPerTile * a.G; t += kTcThreads) {
+                const int r = t % kRowsPerTile, gq = t / kRowsPerTile, i = g.q0 + r;
+                if (i > g.q1) continue;
+                const int hq = g.h * a.G + gq;
+                uint4* op = reinterpret_cast<uint4*>(a.O + (((int64_t)g.b * a.S + i) * a.H + hq) * D);
+                for (int c = 0; c < D / 8; ++c) op[c] = make_uint4(0, 0, 0, 0);
+                if (a.lse) a.lse[((int64_t)g.b * a.H + hq) * a.S + i] = -INFINITY;
+            }
+            return;
         }
-        return;
     }
 
     if (threadIdx.x == 0) {
@@ -258,41 +290,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         for (int i = 0; i < kIdxStages; ++i) {
             mbar_init(bar(kBarIdxFull + i), 32);
-            mbar_init(bar(kBarIdxEmpty + i), kSoftmaxWarps + 2);  // the softmax warps and two copy warps
+            // the softmax warps and the two copy warps (in a pass with one M-tile, the warps of
+            // M-tile A arrive twice)
+            mbar_init(bar(kBarIdxEmpty + i), kSoftmaxWarps + 2);
         }
         mbar_init(bar(kBarQFull), kCopyThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarKFull + i), kCopyThreads);
             mbar_init(bar(kBarVFull + i), kCopyThreads);
+            mbar_init(bar(kBarPFull + i), kRowsPerTile);
+            mbar_init(bar(kBarAFull + i), kRowsPerTile);
+            mbar_init(bar(kBarOReady + i), kRowsPerTile);
         }
-        mbar_init(bar(kBarPFull + 0), 256);
-        mbar_init(bar(kBarPFull + 1), 256);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(kBarStats + i), kRowsPerTile);
         mbar_init_fence();
     }
     if (warp == kMmaWarp) tmem_alloc<512>(smem_u32(tmem_slot));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    // key at position u of the tile's list (gathered keys, then the band); -1 past the end
-    auto key_at = [&](int u) -> int {
-        int j = -1;
-        if (u < n_g) {
-            j = gl[u];
-            if (j < 0 || j >= a.S) {
-                set_status(a.status, DMA_ERR_DEVICE_CHECK);
-                j = -1;
-            }
-        } else if (u < n_all) {
-            j = band_lo + (u - n_g);
-        }
-        return j;
-    };
-
     if (warp == kMetaWarp) {
         // -------------------------------------------------------- key metadata
         regs_decrease<kRegsControl>();
+        const Geom g = tile_geom(a, fresh_ctaid());
+        const int seg = g.seg, q0 = g.q0, q1 = g.q1, W = g.W, nblk = g.nblk, npass = g.npass;
+        auto key_at = [&](int u) { return g.key_at(u, a.S, a.status); };
         const float* sc = a.scores + (int64_t)seg * a.S;
         const int32_t* ex = a.expiry + (int64_t)seg * a.S;
         const int nt = npass * nblk;  // blocks over all passes (every pass walks the same keys)
@@ -350,9 +372,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp >= kCopyWarp0) {
         // -------------------------------------------------------------- copies
         regs_decrease<kRegsControl>();
-        // Each thread copies kCPT consecutive 16-byte chunks of a row (one index load and one
-        // address computation per row for all of them); a sweep covers kRowsPerSweep rows, a
-        // multiple of 8, so the swizzle phase (row mod 8) of a thread's rows never changes.
+        const Geom g = tile_geom(a, fresh_ctaid());
+        const int b = g.b, h = g.h, q0 = g.q0, nblk = g.nblk, npass = g.npass;
+        // Each thread copies kCPT 16-byte chunks of a row (one index load and one address
+        // computation per row for all of them): chunks c0, c0 + kTPR, c0 + 2 kTPR, ... so that the
+        // kTPR threads of a row read kTPR adjacent chunks in each instruction (whole 32-byte
+        // sectors).  A sweep covers kRowsPerSweep rows, a multiple of 8, so the swizzle phase (row
+        // mod 8) of a thread's rows never changes.
         constexpr int kCPR = D / 8;  // 16-byte chunks per row
         constexpr int kCPT = kCopyChunks < kCPR ? kCopyChunks : kCPR;
         constexpr int kTPR = kCPR / kCPT;  // threads per row
@@ -360,11 +386,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr int kSweeps = kBN / kRowsPerSweep;
         static_assert(kRowsPerSweep % 8 == 0 && kBN % kRowsPerSweep == 0, "copy sweep shape");
         const int ct = threadIdx.x - kCopyWarp0 * 32;
-        const int chunk0 = (ct % kTPR) * kCPT, r0 = ct / kTPR;
+        const int chunk0 = ct % kTPR, r0 = ct / kTPR;
         const uint32_t ph = (uint32_t)r0 & 7u;  // swizzle phase of every row this thread copies
         // shared-memory offset of chunk i of this thread within its row
         auto chunk_off = [&](int i) -> uint32_t {
-            const int c = chunk0 + i;
+            const int c = chunk0 + kTPR * i;
             return (uint32_t)((c >> 3) * L::kHalf) + ((((uint32_t)c & 7u) ^ ph) << 4);
         };
         const __nv_bfloat16* Kh = a.K + ((int64_t)b * a.S * a.Hkv + h) * D + chunk0 * 8;
@@ -383,7 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t rb = tile + row * 128;
                 const __nv_bfloat16* src = base + (int64_t)(j >= 0 ? j : 0) * kv_stride;
 #pragma unroll
-                for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * c, j >= 0);
+                for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * kTPR * c, j >= 0);
             }
         };
         bool ok = true;
@@ -400,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t rb = tile + row * 128;
                     const __nv_bfloat16* src = a.Q + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + chunk0 * 8;
 #pragma unroll
-                    for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * c, i < a.S);
+                    for (int c = 0; c < kCPT; ++c) cp_async16(rb + chunk_off(c), src + 8 * kTPR * c, i < a.S);
                 }
             }
             committed(kBarQFull);
@@ -433,219 +459,281 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         cp_async_wait_all();  // the copies already issued land before shared memory goes away
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
+        // The whole warp runs the issue loop with warp-uniform values (the descriptors and
+        // tensor-memory addresses then live in uniform registers) and lane 0 issues each
+        // tcgen05.mma and commit: issuing from a single-thread branch was measured to take about
+        // 110 cycles per MMA, more than the tensor core needs to execute it.
         regs_decrease<kRegsControl>();
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false);
-            constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
-            auto issue_s = [&](int x, int s) {
-                const uint32_t qa = sbase + L::kQ + x * L::kTile, ka = sbase + L::kK + s * L::kTile;
+        const Geom g = tile_geom(a, fresh_ctaid());
+        const int nblk = g.nblk, npass = g.npass;
+        const uint32_t tmem = *tmem_slot;
+        const bool leader = lane == 0;
+        constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false);
+        constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+        // (a descriptor's start address is its low 14 bits, in 16-byte units: the step to the next
+        // 16-element slab is added to the descriptor itself, which never carries out of that field
+        // since shared memory ends below 256 KB)
+        auto issue_s = [&](int x, int s) {
+            const uint64_t dq = smem_desc_sw128(sbase + L::kQ + x * L::kTile, 16, 1024);
+            const uint64_t dk = smem_desc_sw128(sbase + L::kK + s * L::kTile, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * L::kHalf + (kk % 4) * 32;
-                    mma_ss(tmem + 256 + 128 * x, smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(ka + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](int x, int s, bool first) {
-                const uint32_t va = sbase + L::kV + s * L::kTile;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + 128 * x, tmem + 256 + 128 * x + kk * 8, smem_desc_sw128(va + kk * 2048, L::kHalf, 1024),
-                           idO, (first && kk == 0) ? 0u : 1u);
-            };
-            bool ok = true;
-            for (int p = 0; p < npass && ok; ++p) {
-                const int nm = (2 * p + 1 < a.G) ? 2 : 1;
-                if (!(ok = mbar_wait(bar(kBarQFull), p & 1, abort_flag, wait_ns))) break;
-                const int t0 = p * nblk;
-                if (!(ok = mbar_wait(bar(kBarKFull + (t0 & 1)), (t0 >> 1) & 1, abort_flag, wait_ns))) break;
-                fence_proxy_async_smem();  // the cp.async writes (generic proxy) before the MMA reads them
-                tc_fence_after();
-                issue_s(0, t0 & 1);
-                mma_commit(bar(kBarSFull + 0));
-                if (nm == 2) {
-                    issue_s(1, t0 & 1);
-                    mma_commit(bar(kBarSFull + 1));
-                }
-                mma_commit(bar(kBarKEmpty + (t0 & 1)));
-                for (int k = 0; k < nblk; ++k) {
-                    const int t = t0 + k, s = t & 1;
-                    const int t1 = t + 1, s1 = t1 & 1;
-                    // this block's V and the next block's K (both copied by cp.async), then one
-                    // proxy fence for both: their writes must be ordered before the tensor core's reads
-                    if (!(ok = mbar_wait(bar(kBarVFull + s), (t >> 1) & 1, abort_flag, wait_ns))) break;
-                    if (k + 1 < nblk && !(ok = mbar_wait(bar(kBarKFull + s1), (t1 >> 1) & 1, abort_flag, wait_ns)))
-                        break;
-                    fence_proxy_async_smem();
-                    if (!(ok = mbar_wait(bar(kBarPFull + 0), t & 1, abort_flag, wait_ns))) break;
-                    tc_fence_after();
-                    issue_pv(0, s, k == 0);
-                    if (k + 1 < nblk) {
-                        issue_s(0, s1);
-                        mma_commit(bar(kBarSFull + 0));
-                    } else {
-                        mma_commit(bar(kBarOFull + 0));
-                    }
-                    if (nm == 2) {
-                        if (!(ok = mbar_wait(bar(kBarPFull + 1), t & 1, abort_flag, wait_ns))) break;
-                        tc_fence_after();
-                        issue_pv(1, s, k == 0);
-                    }
-                    mma_commit(bar(kBarVEmpty + s));
-                    if (k + 1 < nblk) {
-                        if (nm == 2) {
-                            issue_s(1, s1);
-                            mma_commit(bar(kBarSFull + 1));
-                        }
-                        mma_commit(bar(kBarKEmpty + s1));
-                    } else if (nm == 2) {
-                        mma_commit(bar(kBarOFull + 1));
-                    }
-                }
-                if (ok) mma_commit(bar(kBarQEmpty));
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk / 4) * L::kHalf + (kk % 4) * 32) >> 4;
+                if (leader) mma_ss(tmem + 256 + 128 * x, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
             }
-            // every MMA issued so far has completed before tensor memory is released
-            mma_commit(bar(kBarDrain));
-            mbar_wait_drain(bar(kBarDrain), 0, wait_ns);
+        };
+        auto issue_pv = [&](int x, int s, bool first) {
+            const uint64_t dv = smem_desc_sw128(sbase + L::kV + s * L::kTile, L::kHalf, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                if (leader)
+                    mma_ts(tmem + 128 * x, tmem + 256 + 128 * x + kk * 8, dv + (uint32_t)(kk * (2048 >> 4)), idO,
+                           (first && kk == 0) ? 0u : 1u);
+        };
+        auto commit = [&](int barid) {
+            if (leader) mma_commit(bar(barid));
+        };
+        // PV of M-tile x for block t: P written by the softmax and O rescaled (or, for a pass's
+        // first block, read out by the previous pass's epilogue) by the correction warps
+        auto wait_pv = [&](int x, int t) -> bool {
+            return wait_warp(kBarPFull + x, t & 1) && wait_warp(kBarOReady + x, t & 1);
+        };
+        bool ok = true;
+        for (int p = 0; p < npass && ok; ++p) {
+            const int nm = (2 * p + 1 < a.G) ? 2 : 1;
+            if (!(ok = wait_warp(kBarQFull, p & 1))) break;
+            const int t0 = p * nblk;
+            if (!(ok = wait_warp(kBarKFull + (t0 & 1), (t0 >> 1) & 1))) break;
+            fence_proxy_async_smem();  // the cp.async writes (generic proxy) before the MMA reads them
+            tc_fence_after();
+            issue_s(0, t0 & 1);
+            commit(kBarSFull + 0);
+            if (nm == 2) {
+                issue_s(1, t0 & 1);
+                commit(kBarSFull + 1);
+            }
+            commit(kBarKEmpty + (t0 & 1));
+            for (int k = 0; k < nblk; ++k) {
+                const int t = t0 + k, s = t & 1;
+                const int t1 = t + 1, s1 = t1 & 1;
+                // this block's V and the next block's K (both copied by cp.async), then one proxy
+                // fence for both: their writes must be ordered before the tensor core's reads
+                if (!(ok = wait_warp(kBarVFull + s, (t >> 1) & 1))) break;
+                if (k + 1 < nblk && !(ok = wait_warp(kBarKFull + s1, (t1 >> 1) & 1))) break;
+                fence_proxy_async_smem();
+                if (!(ok = wait_pv(0, t))) break;
+                tc_fence_after();
+                issue_pv(0, s, k == 0);
+                if (k + 1 < nblk) {
+                    issue_s(0, s1);
+                    commit(kBarSFull + 0);
+                } else {
+                    commit(kBarOFull + 0);
+                }
+                if (nm == 2) {
+                    if (!(ok = wait_pv(1, t))) break;
+                    tc_fence_after();
+                    issue_pv(1, s, k == 0);
+                }
+                commit(kBarVEmpty + s);
+                if (k + 1 < nblk) {
+                    if (nm == 2) {
+                        issue_s(1, s1);
+                        commit(kBarSFull + 1);
+                    }
+                    commit(kBarKEmpty + s1);
+                } else if (nm == 2) {
+                    commit(kBarOFull + 1);
+                }
+            }
+            if (ok) commit(kBarQEmpty);
         }
+        // every MMA issued so far has completed before tensor memory is released
+        commit(kBarDrain);
+        if (leader) mbar_wait_drain(bar(kBarDrain), 0, wait_ns);
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------- softmax
-        // Two warpgroups per M-tile: the thread of (row r, half hc) takes columns
-        // [64 hc, 64 hc + 64) of S and P and [D/2 hc, D/2 hc + D/2) of O.  The halves of a
-        // row exchange their block maxima through shared memory (one hardware barrier per
-        // block), so both take exponents against the same running maximum; each keeps its own
-        // part of the row sum, added up at the end.
-        // A wait that runs out never makes a thread leave on its own: the 256 threads of an
-        // M-tile carry their verdict to the next exchange, which ANDs it over all of them, and
-        // leave together.  So no thread is ever left at a hardware barrier that its partners
-        // have walked away from.
-        regs_increase<kRegsSoftmax>();
-        constexpr int kHC = kBN / 2;   // S columns per half
-        constexpr int kHD = D / 2;     // O columns per half
-        const int x = warp >> 3;       // M-tile
-        const int hc = (warp >> 2) & 1;  // column half
-        const int quarter = warp & 3;  // tensor-memory lane quarter
+    } else if (warp >= kCorrWarp0) {
+        // ---------------------------------------------------------- correction
+        // Thread = row r of both M-tiles.  Per block: wait for the softmax's rescale factor of
+        // the row (posted as soon as the block maximum is known), scale the row's O accumulator
+        // in tensor memory when any row of the warp needs it, and release the block's PV.  At the
+        // end of a pass: O / row sum to global memory (bf16) and lse.
+        regs_decrease<kRegsCorr>();
+        const Geom g = tile_geom(a, fresh_ctaid());
+        const int b = g.b, h = g.h, q0 = g.q0, nblk = g.nblk, npass = g.npass;
+        const uint32_t tmem = *tmem_slot;
+        const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const int i = q0 + r;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + 256 + 128 * x + kHC * hc + lane_off;   // this half's S columns
-        const uint32_t tP = tmem + 256 + 128 * x + (kHC / 2) * hc + lane_off;  // this half's P columns
-        const uint32_t tO = tmem + 128 * x + kHD * hc + lane_off;
-        float* xch = reinterpret_cast<float*>(sm + L::kXch) + x * (3 * 2 * kRowsPerTile);  // [slot][half][row]
-        const int col0 = kHC * hc;
         bool ok = true;
-        for (int p = 0; p < npass; ++p) {  // left only by all 256 threads of the M-tile together
+        for (int p = 0; p < npass && ok; ++p) {
             const int nm = (2 * p + 1 < a.G) ? 2 : 1;
-            if (x >= nm) break;
-            const int hq = h * a.G + 2 * p + x;
+            for (int k = 0; k < nblk && ok; ++k) {
+                const int t = p * nblk + k;
+                for (int x = 0; x < nm; ++x) {
+                    if (!(ok = wait_warp(kBarAFull + x, t & 1))) break;
+                    if (k > 0) {
+                        const float alpha = alpha_sm[x * kRowsPerTile + r];
+                        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                            // PV of the previous block has completed: the softmax saw this block's S,
+                            // committed after it
+                            tc_fence_after();
+                            const uint32_t tO = tmem + 128 * x + lane_off;
+                            const f2 al2 = mk2(alpha, alpha);
+#pragma unroll
+                            for (int c0 = 0; c0 < D; c0 += 16) {
+                                uint32_t o0[16];
+                                tmem_ld16(tO + c0, o0);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int e = 0; e < 16; e += 2) {
+                                    float y0, y1;
+                                    split2(mul2(mk2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), al2), y0, y1);
+                                    o0[e] = __float_as_uint(y0);
+                                    o0[e + 1] = __float_as_uint(y1);
+                                }
+                                tmem_st16(tO + c0, o0);
+                            }
+                            tmem_st_wait();
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(bar(kBarOReady + x));
+                }
+            }
+            if (!ok) break;
+            // epilogue of the pass: O = accumulator / row sum
+            for (int x = 0; x < nm; ++x) {
+                const int par = p & 1;
+                ok = wait_warp(kBarStats + 2 * x + par, (p >> 1) & 1) && wait_warp(kBarOFull + x, p & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const float l_row = stats_sm[(par * 2 + x) * kRowsPerTile + r];
+                const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+                const int hq = h * a.G + 2 * p + x;
+                const uint32_t tO = tmem + 128 * x + lane_off;
+                __nv_bfloat16* op = a.O + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {
+                    uint32_t rg[16];
+                    tmem_ld16(tO + 16 * c, rg);
+                    tmem_ld_wait();
+                    if (i < a.S) {
+                        uint4* o4 = reinterpret_cast<uint4*>(op + 16 * c);
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint4 w;
+                            w.x = pack_bf16(__uint_as_float(rg[8 * v + 0]) * inv, __uint_as_float(rg[8 * v + 1]) * inv);
+                            w.y = pack_bf16(__uint_as_float(rg[8 * v + 2]) * inv, __uint_as_float(rg[8 * v + 3]) * inv);
+                            w.z = pack_bf16(__uint_as_float(rg[8 * v + 4]) * inv, __uint_as_float(rg[8 * v + 5]) * inv);
+                            w.w = pack_bf16(__uint_as_float(rg[8 * v + 6]) * inv, __uint_as_float(rg[8 * v + 7]) * inv);
+                            o4[v] = w;
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------- softmax
+        // Thread = one query row of M-tile x (tensor-memory lane r): the 128 logits of a block
+        // in registers, the exact block maximum, the rescale factor posted for the correction
+        // warps, then the exponentials written back as bf16 P over S.
+        regs_increase<kRegsSoftmax>();
+        const Geom g = tile_geom(a, fresh_ctaid());
+        const int q0 = g.q0, W = g.W, nblk = g.nblk, npass = g.npass;
+        const uint32_t tmem = *tmem_slot;
+        const int x = warp >> 2;  // M-tile
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int i = q0 + r;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + 256 + 128 * x + lane_off;
+        const f2 cc2 = mk2(a.c_log2, a.c_log2);
+        bool ok = true;
+        for (int p = 0; p < npass && ok; ++p) {
+            const int nm = (2 * p + 1 < a.G) ? 2 : 1;
+            if (x >= nm) break;  // M-tile B has no query head in the last pass of an odd group
+            const uint32_t idx_arrivals = nm == 1 ? 2u : 1u;  // M-tile A then arrives for both
             float m_used = -INFINITY, l = 0.f;
             for (int k = 0; k < nblk; ++k) {
                 const int t = p * nblk + k;
                 const int ridx = t % kIdxStages;
-                // (after a failed wait the rest of the block runs on stale data: nothing it reads
-                // or writes leaves this CTA's shared and tensor memory, and the exchange below
-                // ends the pass)
-                ok = ok && wait_warp(kBarIdxFull + ridx, (t / kIdxStages) & 1);
-                ok = ok && wait_warp(kBarSFull + x, t & 1);
+                ok = wait_warp(kBarIdxFull + ridx, (t / kIdxStages) & 1) && wait_warp(kBarSFull + x, t & 1);
+                if (!ok) break;
                 tc_fence_after();
                 const int* js = idx_slot(ridx);
-                const float* mb = reinterpret_cast<const float*>(js + kBN) + col0;
+                const float* mb = reinterpret_cast<const float*>(js + kBN);
                 const int all_full = js[5 * kBN];
-                // keep bits of this row for a block that needs a mask (computed before S is held
-                // in registers): kept iff j <= i < j + window  or  lo_j <= i < expiry_j
-                uint32_t kbits[kHC / 32] = {~0u, ~0u};
-                if (!all_full) {
-                    const int* mj = js + 2 * kBN + col0;
-                    const int* mlo = js + 3 * kBN + col0;
-                    const int* mtl = js + 4 * kBN + col0;
-#pragma unroll
-                    for (int w32 = 0; w32 < kHC / 32; ++w32) {
-                        uint32_t bits = 0;
-#pragma unroll
-                        for (int cc = 0; cc < 32; cc += 4) {
-                            const int c = 32 * w32 + cc;
-                            const int4 jj = *reinterpret_cast<const int4*>(mj + c);
-                            const int4 lo = *reinterpret_cast<const int4*>(mlo + c);
-                            const int4 tl = *reinterpret_cast<const int4*>(mtl + c);
-                            bits |= (((unsigned)(i - jj.x) < (unsigned)W || (unsigned)(i - lo.x) < (unsigned)tl.x) ? 1u : 0u) << cc;
-                            bits |= (((unsigned)(i - jj.y) < (unsigned)W || (unsigned)(i - lo.y) < (unsigned)tl.y) ? 2u : 0u) << cc;
-                            bits |= (((unsigned)(i - jj.z) < (unsigned)W || (unsigned)(i - lo.z) < (unsigned)tl.z) ? 4u : 0u) << cc;
-                            bits |= (((unsigned)(i - jj.w) < (unsigned)W || (unsigned)(i - lo.w) < (unsigned)tl.w) ? 8u : 0u) << cc;
-                        }
-                        kbits[w32] = bits;
-                    }
-                }
-                // this half of the S row: two loads in flight, one wait
-                float xv[kHC];
-                {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tS + 0, r0);
-                    tmem_ld32(tS + 32, r1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        xv[e] = __uint_as_float(r0[e]);
-                        xv[32 + e] = __uint_as_float(r1[e]);
-                    }
-                }
+                float xv[kBN];
+                tmem_ld32f(tS + 0, xv);
+                tmem_ld32f(tS + 32, xv + 32);
+                tmem_ld32f(tS + 64, xv + 64);
+                tmem_ld32f(tS + 96, xv + 96);
+                tmem_ld_wait();
                 // logits in log2 units: x = S * scale * log2(e) + bias * log2(e)
-                const f2 cc2 = mk2(a.c_log2, a.c_log2);
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (all_full) {
 #pragma unroll
-                for (int c = 0; c < kHC; c += 4) {
-                    const float4 bb = *reinterpret_cast<const float4*>(mb + c);
-                    f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
-                    f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
-                    split2(x01, xv[c], xv[c + 1]);
-                    split2(x23, xv[c + 2], xv[c + 3]);
-                    if (!all_full) {
-                        const uint32_t bits = kbits[c / 32] >> (c % 32);
-                        if (!(bits & 1u)) xv[c] = -INFINITY;
-                        if (!(bits & 2u)) xv[c + 1] = -INFINITY;
-                        if (!(bits & 4u)) xv[c + 2] = -INFINITY;
-                        if (!(bits & 8u)) xv[c + 3] = -INFINITY;
+                    for (int c = 0; c < kBN; c += 4) {
+                        const float4 bb = *reinterpret_cast<const float4*>(mb + c);
+                        f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
+                        f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
+                        split2(x01, xv[c], xv[c + 1]);
+                        split2(x23, xv[c + 2], xv[c + 3]);
+                        const int q = (c / 4) & 3;
+                        mx[q] = max3(mx[q], xv[c], xv[c + 1]);
+                        mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
                     }
-                    const int q = (c / 4) & 3;
-                    mx[q] = max3(mx[q], xv[c], xv[c + 1]);
-                    mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
+                } else {
+                    // kept iff j <= i < j + window  or  lo_j <= i < expiry_j
+                    const int* mj = js + 2 * kBN;
+                    const int* mlo = js + 3 * kBN;
+                    const int* mtl = js + 4 * kBN;
+#pragma unroll
+                    for (int c = 0; c < kBN; c += 4) {
+                        const float4 bb = *reinterpret_cast<const float4*>(mb + c);
+                        const int4 jj = *reinterpret_cast<const int4*>(mj + c);
+                        const int4 lo = *reinterpret_cast<const int4*>(mlo + c);
+                        const int4 tl = *reinterpret_cast<const int4*>(mtl + c);
+                        f2 x01 = fma2(mk2(xv[c], xv[c + 1]), cc2, mk2(bb.x, bb.y));
+                        f2 x23 = fma2(mk2(xv[c + 2], xv[c + 3]), cc2, mk2(bb.z, bb.w));
+                        split2(x01, xv[c], xv[c + 1]);
+                        split2(x23, xv[c + 2], xv[c + 3]);
+                        if (!((unsigned)(i - jj.x) < (unsigned)W || (unsigned)(i - lo.x) < (unsigned)tl.x)) xv[c] = -INFINITY;
+                        if (!((unsigned)(i - jj.y) < (unsigned)W || (unsigned)(i - lo.y) < (unsigned)tl.y)) xv[c + 1] = -INFINITY;
+                        if (!((unsigned)(i - jj.z) < (unsigned)W || (unsigned)(i - lo.z) < (unsigned)tl.z)) xv[c + 2] = -INFINITY;
+                        if (!((unsigned)(i - jj.w) < (unsigned)W || (unsigned)(i - lo.w) < (unsigned)tl.w)) xv[c + 3] = -INFINITY;
+                        const int q = (c / 4) & 3;
+                        mx[q] = max3(mx[q], xv[c], xv[c + 1]);
+                        mx[q] = max3(mx[q], xv[c + 2], xv[c + 3]);
+                    }
                 }
-                // block maximum of the whole row: exchange with the other half
-                float m_blk = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
-                {
-                    // (the barrier also orders this half's S loads before the other half's P
-                    // stores, which land in tensor-memory columns that held this half's S)
-                    float* xb = xch + (t & 1) * (2 * kRowsPerTile);
-                    xb[hc * kRowsPerTile + r] = m_blk;
-                    tc_fence_before();
-                    ok = named_bar_and(1 + x, 256, ok);  // the same verdict for both halves
-                    tc_fence_after();
-                    if (!ok) break;
-                    m_blk = fmaxf(m_blk, xb[(1 - hc) * kRowsPerTile + r]);
-                }
-                // The maximum of a row moved up: what it has accumulated is rescaled below.
-                const bool raise = m_blk > m_used + kRescaleThreshold;
+                const float m_blk = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+                // The maximum of the row moved up: what O has accumulated is rescaled by the
+                // correction warps while the exponentials are computed here.
+                const bool raise = m_blk > m_used;
                 const bool rescale = raise && k > 0 && m_used != -INFINITY;
                 const float alpha = rescale ? ex2(m_used - m_blk) : 1.f;
                 if (raise) m_used = m_blk;
+                alpha_sm[x * kRowsPerTile + r] = alpha;
+                tc_fence_before();
+                mbar_arrive(bar(kBarAFull + x));
                 const float m_eff = m_used == -INFINITY ? 0.f : m_used;
                 const f2 me2 = mk2(m_eff, m_eff);
                 f2 ls[4] = {mk2(0.f, 0.f), mk2(0.f, 0.f), mk2(0.f, 0.f), mk2(0.f, 0.f)};
 #pragma unroll
-                for (int c0 = 0; c0 < kHC; c0 += 32) {
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float a0, a1;
                         split2(sub2(mk2(xv[c0 + 2 * e], xv[c0 + 2 * e + 1]), me2), a0, a1);
-                        // a share of the exponentials goes to the FMA pipe, the rest to the MUFU
-                        const bool poly = kPolyEvery > 0 && (e % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1;
-                        const float p0 = poly ? ex2_poly(a0) : ex2(a0);
-                        const float p1 = poly ? ex2_poly(a1) : ex2(a1);
+                        const float p0 = ex2(a0), p1 = ex2(a1);
                         ls[e & 3] = add2(ls[e & 3], mk2(p0, p1));
                         pk[e] = pack_bf16(p0, p1);
                     }
-                    tmem_st16(tP + c0 / 2, pk);
+                    tmem_st16(tS + c0 / 2, pk);
                 }
                 {
                     const f2 tt = add2(add2(ls[0], ls[1]), add2(ls[2], ls[3]));
@@ -653,70 +741,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     split2(tt, t0, t1);
                     l = l * alpha + (t0 + t1);
                 }
-                // O *= alpha for the rows whose maximum moved (tcgen05.ld/st are warp-collective:
-                // the warp does it when any of its rows needs it, with factor 1 for the others).
-                // PV of the previous block has completed: its commit preceded this block's S.
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const f2 al2 = mk2(alpha, alpha);
-#pragma unroll
-                    for (int c0 = 0; c0 < kHD; c0 += 32) {
-                        uint32_t o0[32];
-                        tmem_ld32(tO + c0, o0);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            f2 v0 = mul2(mk2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), al2);
-                            float y0, y1;
-                            split2(v0, y0, y1);
-                            o0[e] = __float_as_uint(y0);
-                            o0[e + 1] = __float_as_uint(y1);
-                        }
-                        tmem_st32(tO + c0, o0);
-                    }
-                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(kBarPFull + x));
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarIdxEmpty + ridx));  // done with this block's metadata
+                if (lane == 0) mbar_arrive_cnt(bar(kBarIdxEmpty + ridx), idx_arrivals);  // done with the metadata
             }
             if (!ok) break;
-            // epilogue: O = accumulator / (sum of both halves' row sums)
-            float l_row;
-            {
-                float* xb = xch + 2 * (2 * kRowsPerTile);  // its own slot: the blocks use slots 0 and 1
-                xb[hc * kRowsPerTile + r] = l;
-                named_bar_sync(1 + x, 256);
-                l_row = l + xb[(1 - hc) * kRowsPerTile + r];
-                named_bar_sync(1 + x, 256);  // both halves have read before the slot is reused
-            }
-            // (on a failed wait the store is skipped and the next pass's first exchange ends
-            // the loop for both halves)
-            if (!(ok = wait_warp(kBarOFull + x, p & 1))) continue;
-            tc_fence_after();
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            __nv_bfloat16* op = a.O + (((int64_t)b * a.S + min(i, a.S - 1)) * a.H + hq) * D + kHD * hc;
-#pragma unroll
-            for (int c = 0; c < kHD / 32; ++c) {
-                uint32_t rg[32];
-                tmem_ld32(tO + 32 * c, rg);
-                tmem_ld_wait();
-                if (i < a.S) {
-                    uint4* o4 = reinterpret_cast<uint4*>(op + 32 * c);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(rg[8 * v + 0]) * inv, __uint_as_float(rg[8 * v + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(rg[8 * v + 2]) * inv, __uint_as_float(rg[8 * v + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(rg[8 * v + 4]) * inv, __uint_as_float(rg[8 * v + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(rg[8 * v + 6]) * inv, __uint_as_float(rg[8 * v + 7]) * inv);
-                        o4[v] = w;
-                    }
-                }
-            }
-            if (a.lse && hc == 0 && i < a.S)
-                a.lse[((int64_t)b * a.H + hq) * a.S + i] = l_row > 0.f ? (m_used + __log2f(l_row)) * kLn2 : -INFINITY;
-            tc_fence_before();
+            // the pass's row sum for the correction warps' epilogue, and lse
+            stats_sm[((p & 1) * 2 + x) * kRowsPerTile + r] = l;
+            mbar_arrive(bar(kBarStats + 2 * x + (p & 1)));
+            if (a.lse && i < a.S)
+                a.lse[((int64_t)g.b * a.H + g.h * a.G + 2 * p + x) * a.S + i] =
+                    l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
         }
     }
 
@@ -724,7 +761,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) tmem_dealloc<512>(tmem);
+    if (warp == kMmaWarp) tmem_dealloc<512>(*tmem_slot);
 }
 
 template <int D>

@@ -127,6 +127,10 @@ EDGE = [
     (1, 384, 4, 2, 128, torch.bfloat16, 0, 100, 1, 0),
     (1, 450, 4, 2, 128, torch.bfloat16, 30, 0, 1, 1),
     (1, 1100, 4, 2, 64, torch.bfloat16, 256, 64, 64, 0),
+    # one query head per KV head, and an odd group, each with more key blocks than the
+    # metadata ring holds (the idle M-tile's share of the ring's releases)
+    (1, 2048, 2, 2, 128, torch.bfloat16, 512, 64, 1, 0),
+    (1, 1500, 3, 1, 128, torch.bfloat16, 400, 100, 1, 0),
 ]
 
 
