@@ -78,16 +78,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum : int {
     kBarQFull = 0,
     kBarQEmpty = 1,
-    kBarKFull = 2,    // 2 stages
+    kBarK0Full = 2,   // the K rows of a pass's first block have landed
     kBarKEmpty = 4,   // 2 stages
-    kBarVFull = 6,    // 2 stages
+    kBarBlkFull = 6,  // 2 stages (block t: t & 1): the V rows of block t and the K rows of block t + 1
     kBarVEmpty = 8,   // 2 stages
     kBarSFull = 10,   // per M-tile: S of a block is in tensor memory
-    kBarPFull = 12,   // per M-tile: P of a block is in tensor memory
+    kBarPFull = 12,   // per M-tile: P of a block is in tensor memory (softmax) and O is rescaled
+                      // for it, or read out by the previous pass's epilogue (correction)
     kBarOFull = 14,   // per M-tile: the last PV of a pass has completed
     kBarDrain = 16,
     kBarAFull = 17,   // per M-tile: the rescale factors of a block are in shared memory
-    kBarOReady = 19,  // per M-tile: O is rescaled for a block (or drained, for a pass's first block)
     kBarStats = 21,   // per (M-tile, pass parity): the row sums of a pass are in shared memory
     kBarIdxFull = 25,  // kIdxStages slots
     kBarIdxEmpty = 25 + kIdxStages,
@@ -295,12 +295,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(kBarIdxEmpty + i), kSoftmaxWarps + 2);
         }
         mbar_init(bar(kBarQFull), kCopyThreads);
+        mbar_init(bar(kBarK0Full), kCopyThreads);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kBarKFull + i), kCopyThreads);
-            mbar_init(bar(kBarVFull + i), kCopyThreads);
-            mbar_init(bar(kBarPFull + i), kRowsPerTile);
+            mbar_init(bar(kBarBlkFull + i), kCopyThreads);
+            mbar_init(bar(kBarPFull + i), 2 * kRowsPerTile);
             mbar_init(bar(kBarAFull + i), kRowsPerTile);
-            mbar_init(bar(kBarOReady + i), kRowsPerTile);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(kBarStats + i), kRowsPerTile);
         mbar_init_fence();
@@ -431,29 +430,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             committed(kBarQFull);
             const int t0 = p * nblk;
+            // copies of the K rows of block t into stage t & 1 (no completion signal of their own)
             auto load_k = [&](int t) -> bool {
                 const int s = t & 1, use = t >> 1, r = t % kIdxStages;
                 if (!acquire(kBarIdxFull + r, (t / kIdxStages) & 1)) return false;
                 if (use >= 1 && !acquire(kBarKEmpty + s, (use - 1) & 1)) return false;
                 copy_rows(sbase + L::kK + s * L::kTile, idx_slot(r), Kh);
-                // (fault injection for tests: the MMA warp's wait for these rows then runs out)
-                if (!(kFaultTest && test_drop_arrive && blockIdx.x == 0 && t == 0)) committed(kBarKFull + s);
                 return true;
             };
             auto load_v = [&](int t) -> bool {
                 const int s = t & 1, use = t >> 1, r = t % kIdxStages;
                 if (use >= 1 && !acquire(kBarVEmpty + s, (use - 1) & 1)) return false;
                 copy_rows(sbase + L::kV + s * L::kTile, idx_slot(r), Vh);
-                committed(kBarVFull + s);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(kBarIdxEmpty + r));  // done with this slot's indices
                 return true;
             };
-            // V of a block is needed (by PV) before K of the next one (by the next S)
             ok = load_k(t0);
+            // (fault injection for tests: the MMA warp's wait for these rows then runs out)
+            if (ok && !(kFaultTest && test_drop_arrive && blockIdx.x == 0 && p == 0)) committed(kBarK0Full);
+            // V of a block is needed (by PV) before K of the next one (by the next S); one
+            // completion signal covers both
             for (int k = 0; k < nblk && ok; ++k) {
                 ok = load_v(t0 + k);
                 if (ok && k + 1 < nblk) ok = load_k(t0 + k + 1);
+                if (ok) committed(kBarBlkFull + ((t0 + k) & 1));
             }
         }
         cp_async_wait_all();  // the copies already issued land before shared memory goes away
@@ -495,15 +496,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         // PV of M-tile x for block t: P written by the softmax and O rescaled (or, for a pass's
         // first block, read out by the previous pass's epilogue) by the correction warps
-        auto wait_pv = [&](int x, int t) -> bool {
-            return wait_warp(kBarPFull + x, t & 1) && wait_warp(kBarOReady + x, t & 1);
-        };
+        auto wait_pv = [&](int x, int t) -> bool { return wait_warp(kBarPFull + x, t & 1); };
         bool ok = true;
         for (int p = 0; p < npass && ok; ++p) {
             const int nm = (2 * p + 1 < a.G) ? 2 : 1;
             if (!(ok = wait_warp(kBarQFull, p & 1))) break;
             const int t0 = p * nblk;
-            if (!(ok = wait_warp(kBarKFull + (t0 & 1), (t0 >> 1) & 1))) break;
+            if (!(ok = wait_warp(kBarK0Full, p & 1))) break;
             fence_proxy_async_smem();  // the cp.async writes (generic proxy) before the MMA reads them
             tc_fence_after();
             issue_s(0, t0 & 1);
@@ -518,8 +517,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int t1 = t + 1, s1 = t1 & 1;
                 // this block's V and the next block's K (both copied by cp.async), then one proxy
                 // fence for both: their writes must be ordered before the tensor core's reads
-                if (!(ok = wait_warp(kBarVFull + s, (t >> 1) & 1))) break;
-                if (k + 1 < nblk && !(ok = wait_warp(kBarKFull + s1, (t1 >> 1) & 1))) break;
+                if (!(ok = wait_warp(kBarBlkFull + s, (t >> 1) & 1))) break;
                 fence_proxy_async_smem();
                 if (!(ok = wait_pv(0, t))) break;
                 tc_fence_after();
@@ -599,7 +597,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                     tc_fence_before();
-                    mbar_arrive(bar(kBarOReady + x));
+                    mbar_arrive(bar(kBarPFull + x));
                 }
             }
             if (!ok) break;
