@@ -43,8 +43,9 @@ struct SelectPlan {
     int nC;         // ceil(n / T)
     int X;          // position block length of the 2-D count table
     int nX;         // ceil(n / X)
+    int nlc;        // list chunks per segment (of the key and rank-order compactions)
     // byte offsets into the workspace
-    size_t off_key[2], off_val[2], off_hist, off_rank, off_tab, off_f0, off_bval, off_bexp;
+    size_t off_key[2], off_val[2], off_hist, off_rank, off_tab, off_f0, off_bval, off_bexp, off_lcnt, off_krn;
     size_t bytes;
 };
 

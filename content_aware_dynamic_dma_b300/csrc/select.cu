@@ -484,122 +484,287 @@ __global__ void expand_block_kernel(const int32_t* __restrict__ bexp, int S, int
 }
 
 // ------------------------------------------------------------ compaction ------
+//
+// Three lists per segment, each written in two launches over chunks of kListChunk
+// (counts, then writes at offsets summed from the counts of the chunks before):
+//   idx      keys ever in the top set (lo_j < expiry_j), ascending
+//   top_idx  keys in the top set of the last row (expiry_j >= S), ascending
+//   kr       units ever in the top set, in rank order (best first), with their
+//            expiry: the per-tile key lists are filtered from it
+// A unit is one key (token units) or one block of `block` keys, whose keys share
+// one interval.
 
-constexpr int kCompactThreads = 1024;
-// Per segment, in key order: idx <- keys ever in the top set; top <- keys in the
-// top set of the last row.
-__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const int32_t* __restrict__ expiry, int S,
-                                                                  int block, int32_t* __restrict__ idx,
-                                                                  int32_t* __restrict__ count,
-                                                                  int32_t* __restrict__ top_idx,
-                                                                  int32_t* __restrict__ top_count, int top_cap,
+constexpr int kListChunk = 4096;
+constexpr int kListThreads = 512;
+constexpr int kListPer = kListChunk / kListThreads;  // consecutive items per thread
+
+// Block-wide exclusive scan of two counters per thread (blockDim.x a multiple of
+// 32, <= 1024); totals in *tot.
+__device__ int2 block_exclusive_scan2(int2 v, int2* warp_buf, int2* tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int2 x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int yx = __shfl_up_sync(0xffffffffu, x.x, o), yy = __shfl_up_sync(0xffffffffu, x.y, o);
+        if (lane >= o) {
+            x.x += yx;
+            x.y += yy;
+        }
+    }
+    if (lane == 31) warp_buf[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int2 t = lane < nw ? warp_buf[lane] : make_int2(0, 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yx = __shfl_up_sync(0xffffffffu, t.x, o), yy = __shfl_up_sync(0xffffffffu, t.y, o);
+            if (lane >= o) {
+                t.x += yx;
+                t.y += yy;
+            }
+        }
+        warp_buf[lane] = t;
+    }
+    __syncthreads();
+    const int2 w0 = warp > 0 ? warp_buf[warp - 1] : make_int2(0, 0);
+    *tot = warp_buf[nw - 1];
+    __syncthreads();
+    return make_int2(w0.x + x.x - v.x, w0.y + x.y - v.y);
+}
+
+struct ListItems {
+    int ever[kListPer], last[kListPer], kr[kListPer];  // flags
+    int kr_u[kListPer], kr_e[kListPer];
+};
+
+// Flags of this thread's items of chunk c: keys c*kListChunk + kListPer*tid + i (index
+// order) and ranks likewise (rank order).
+__device__ __forceinline__ void list_items(const int32_t* ex, const int32_t* p, int S, int n, int block, int c,
+                                           ListItems& it, int* status)
+{
+    const int base = c * kListChunk + kListPer * (int)threadIdx.x;
+    const int bs = block <= 1 ? 1 : block;
+#pragma unroll
+    for (int i = 0; i < kListPer; ++i) {
+        const int j = base + i;
+        const int e = j < S ? ex[j] : 0;
+        const int ever = (j < S && top_lo(j, block) < e) ? 1 : 0;
+        it.ever[i] = ever;
+        it.last[i] = (ever && e >= S) ? 1 : 0;
+        const int r = base + i;
+        int u = -1, eu = 0, kr = 0;
+        if (r < n) {
+            u = p[r];
+            if (u < 0 || u >= n) {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+            } else {
+                eu = ex[(int64_t)u * bs];
+                kr = top_lo(u * bs, block) < eu ? 1 : 0;
+            }
+        }
+        it.kr[i] = kr;
+        it.kr_u[i] = u;
+        it.kr_e[i] = eu;
+    }
+}
+
+// cnt[seg][chunk] = (ever, last, kr) counts of the chunk.
+__global__ void __launch_bounds__(kListThreads) list_count_kernel(const int32_t* __restrict__ expiry,
+                                                                  const int32_t* __restrict__ p, int S, int n,
+                                                                  int block, int nlc, int4* __restrict__ cnt,
                                                                   int* status)
 {
-    __shared__ int warp_buf[32];
-    const int seg = blockIdx.x;
-    const int32_t* ex = expiry + (int64_t)seg * S;
-    int run_all = 0, run_top = 0;
-    for (int base = 0; base < S; base += kCompactThreads) {
-        const int j = base + threadIdx.x;
-        int lo = top_lo(j, block);
-        int e = j < S ? ex[j] : 0;
-        int ever = (j < S && lo < e) ? 1 : 0;
-        int last = (ever && e >= S) ? 1 : 0;
-        int tot_all, tot_top;
-        int b_all = block_exclusive_scan(ever, warp_buf, &tot_all);
-        int b_top = block_exclusive_scan(last, warp_buf, &tot_top);
-        if (ever) idx[(int64_t)seg * S + run_all + b_all] = j;
-        if (last && top_idx) {
-            int o = run_top + b_top;
-            if (o < top_cap)
-                top_idx[(int64_t)seg * top_cap + o] = j;
+    __shared__ int4 red[kListThreads / 32];
+    const int seg = blockIdx.y, c = blockIdx.x;
+    ListItems it;
+    list_items(expiry + (int64_t)seg * S, p + (int64_t)seg * n, S, n, block, c, it, status);
+    int a = 0, l = 0, k = 0;
+#pragma unroll
+    for (int i = 0; i < kListPer; ++i) {
+        a += it.ever[i];
+        l += it.last[i];
+        k += it.kr[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        l += __shfl_xor_sync(0xffffffffu, l, o);
+        k += __shfl_xor_sync(0xffffffffu, k, o);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) red[warp] = make_int4(a, l, k, 0);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int4 t = make_int4(0, 0, 0, 0);
+        for (int w = 0; w < kListThreads / 32; ++w) {
+            t.x += red[w].x;
+            t.y += red[w].y;
+            t.z += red[w].z;
+        }
+        cnt[(int64_t)seg * nlc + c] = t;
+    }
+}
+
+__global__ void __launch_bounds__(kListThreads) list_write_kernel(
+    const int32_t* __restrict__ expiry, const int32_t* __restrict__ p, int S, int n, int block, int nlc,
+    const int4* __restrict__ cnt, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+    int32_t* __restrict__ top_idx, int32_t* __restrict__ top_count, int top_cap, int32_t* __restrict__ kr_u,
+    int32_t* __restrict__ kr_e, int32_t* __restrict__ kr_n, int* status)
+{
+    __shared__ int2 warp_buf[32];
+    __shared__ int4 off_s;
+    const int seg = blockIdx.y, c = blockIdx.x;
+    // offsets: the counts of the chunks before this one
+    if (threadIdx.x < 32) {
+        int a = 0, l = 0, k = 0;
+        for (int q = threadIdx.x; q < c; q += 32) {
+            const int4 v = cnt[(int64_t)seg * nlc + q];
+            a += v.x;
+            l += v.y;
+            k += v.z;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            l += __shfl_xor_sync(0xffffffffu, l, o);
+            k += __shfl_xor_sync(0xffffffffu, k, o);
+        }
+        if (threadIdx.x == 0) off_s = make_int4(a, l, k, 0);
+    }
+    ListItems it;
+    list_items(expiry + (int64_t)seg * S, p + (int64_t)seg * n, S, n, block, c, it, status);
+    int a = 0, l = 0, k = 0;
+#pragma unroll
+    for (int i = 0; i < kListPer; ++i) {
+        a += it.ever[i];
+        l += it.last[i];
+        k += it.kr[i];
+    }
+    int2 tot;
+    const int2 b_al = block_exclusive_scan2(make_int2(a, l), warp_buf, &tot);
+    const int b_k = block_exclusive_scan2(make_int2(k, 0), warp_buf, &tot).x;
+    const int4 off = off_s;
+    const int base = c * kListChunk + kListPer * (int)threadIdx.x;
+    int oa = off.x + b_al.x, ol = off.y + b_al.y, ok = off.z + b_k;
+#pragma unroll
+    for (int i = 0; i < kListPer; ++i) {
+        const int j = base + i;
+        if (it.ever[i]) idx[(int64_t)seg * S + oa++] = j;
+        if (it.last[i] && top_idx) {
+            if (ol < top_cap)
+                top_idx[(int64_t)seg * top_cap + ol] = j;
             else
                 set_status(status, DMA_ERR_DEVICE_CHECK);
+            ++ol;
         }
-        run_all += tot_all;
-        run_top += tot_top;
+        if (it.kr[i]) {
+            kr_u[(int64_t)seg * n + ok] = it.kr_u[i];
+            kr_e[(int64_t)seg * n + ok] = it.kr_e[i];
+            ++ok;
+        }
     }
-    if (threadIdx.x == 0) {
-        count[seg] = run_all;
-        if (top_count) top_count[seg] = min(run_top, top_cap);
+    if (c == nlc - 1 && threadIdx.x == kListThreads - 1) {
+        count[seg] = oa;
+        if (top_count) top_count[seg] = min(ol, top_cap);
+        kr_n[seg] = ok;
     }
 }
 
 // ----------------------------------------------------------- per-tile lists ---
 
 constexpr int kTileThreads = 256;
-constexpr int kTilePartialCap = 1024;  // keys kept by only some rows of a tile (at most ~256 by construction)
+constexpr int kTilePer = 8;            // consecutive list entries per thread per sweep
+constexpr int kTilePartialCap = 1024;  // keys kept by only some rows of a tile (at most ~384 by construction)
 // For query tile [q0, q1]: keys j <= lim (lim = q0 - window, or q1 without a
 // window) with lo_j <= q1 and expiry_j > q0.  The keys kept by every row of the
-// tile (lo_j <= q0 and expiry_j > q1) come first, ascending, then the keys kept
-// by only some of its rows, ascending: a consumer that walks the list in blocks
-// finds the blocks that need a per-row mask at the end.  Also the bitmap of
-// 64-key blocks holding a kept key (gathered keys and the window band).
-__global__ void __launch_bounds__(kTileThreads) tile_list_kernel(const int32_t* __restrict__ expiry,
-                                                                 const int32_t* __restrict__ idx,
-                                                                 const int32_t* __restrict__ count, int S, int block,
-                                                                 int window, int n_qt, int tile_stride,
-                                                                 int bitmap_words, int32_t* __restrict__ tile_cnt,
-                                                                 int32_t* __restrict__ tile_idx,
-                                                                 uint32_t* __restrict__ bitmap, int* status)
+// tile (lo_j <= q0 and expiry_j > q1) come first, then the keys kept by only some
+// of its rows; each group in rank order (best unit first; the keys of a block
+// ascending), so that a consumer walking the list in blocks meets the keys most
+// likely to hold a row's maximum first and finds the blocks that need a per-row
+// mask at the end.  Also the bitmap of 64-key blocks holding a kept key
+// (gathered keys and the window band).
+__global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
+    const int32_t* __restrict__ kr_u, const int32_t* __restrict__ kr_e, const int32_t* __restrict__ kr_n, int S,
+    int n, int block, int window, int n_qt, int tile_stride, int bitmap_words, int32_t* __restrict__ tile_cnt,
+    int32_t* __restrict__ tile_idx, uint32_t* __restrict__ bitmap, int* status)
 {
     extern __shared__ uint32_t bm[];  // [bitmap_words]
-    __shared__ int warp_buf[32];
+    __shared__ int2 warp_buf[32];
     __shared__ int part_s[kTilePartialCap];
-    __shared__ int stop;
     const int seg = blockIdx.y, tile = blockIdx.x;
     const int q0 = tile * kQTile, q1 = min(S, q0 + kQTile) - 1;
     const int lim = window > 0 ? q0 - window : q1;
-    const int32_t* ex = expiry + (int64_t)seg * S;
-    const int32_t* li = idx + (int64_t)seg * S;
-    const int n = count[seg];
+    const int bs = block <= 1 ? 1 : block;
+    const int32_t* ku = kr_u + (int64_t)seg * n;
+    const int32_t* ke = kr_e + (int64_t)seg * n;
+    const int m = min(max(kr_n[seg], 0), n);
     int32_t* out = tile_idx + ((int64_t)seg * n_qt + tile) * tile_stride;
     if (bitmap)
         for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bm[t] = 0;
-    if (threadIdx.x == 0) stop = 0;
     __syncthreads();
     int run_full = 0, run_part = 0;
-    for (int base = 0; base < n; base += kTileThreads) {
-        const int u = base + threadIdx.x;
-        int j = u < n ? li[u] : INT32_MAX;
-        int act_full = 0, act_part = 0;
-        if (j < 0 || (j >= S && j != INT32_MAX)) {
-            set_status(status, DMA_ERR_DEVICE_CHECK);
-            j = INT32_MAX;
-        }
-        if (j <= lim) {
-            const int e = ex[j], lo = top_lo(j, block);
-            if (lo <= q1 && e > q0) {
-                if (lo <= q0 && e > q1)
-                    act_full = 1;
-                else
-                    act_part = 1;
+    for (int base = 0; base < m; base += kTileThreads * kTilePer) {
+        const int e0 = base + kTilePer * (int)threadIdx.x;
+        int nk[kTilePer];  // keys of the entry in the tile's list (0: none), full in the high bit
+        int u0[kTilePer];
+        int full = 0, part = 0;
+#pragma unroll
+        for (int i = 0; i < kTilePer; ++i) {
+            nk[i] = 0;
+            u0[i] = 0;
+            const int q = e0 + i;
+            if (q < m) {
+                const int u = ku[q], e = ke[q];
+                const int j0 = u * bs;
+                const int lo = top_lo(j0, block);
+                if (u < 0 || j0 >= S) {
+                    set_status(status, DMA_ERR_DEVICE_CHECK);
+                } else if (lo <= q1 && e > q0 && j0 <= lim) {
+                    const int c = min(bs, lim - j0 + 1);  // the block's keys up to lim
+                    const bool f = lo <= q0 && e > q1;
+                    nk[i] = c | (f ? (1 << 30) : 0);
+                    u0[i] = j0;
+                    if (f)
+                        full += c;
+                    else
+                        part += c;
+                }
             }
         }
-        if (u < n && j > lim) stop = 1;  // the list is ascending: nothing later qualifies
-        int tot_full, tot_part;
-        const int before_full = block_exclusive_scan(act_full, warp_buf, &tot_full);
-        const int before_part = block_exclusive_scan(act_part, warp_buf, &tot_part);
-        if (act_full) {
-            const int o = run_full + before_full;
-            if (o < tile_stride)
-                out[o] = j;
-            else
-                set_status(status, DMA_ERR_DEVICE_CHECK);
+        int2 tot;
+        const int2 before = block_exclusive_scan2(make_int2(full, part), warp_buf, &tot);
+        int of = run_full + before.x, op = run_part + before.y;
+#pragma unroll
+        for (int i = 0; i < kTilePer; ++i) {
+            const int c = nk[i] & ((1 << 30) - 1);
+            if (c == 0) continue;
+            const bool f = (nk[i] >> 30) != 0;
+            for (int q = 0; q < c; ++q) {
+                const int j = u0[i] + q;
+                if (f) {
+                    if (of < tile_stride)
+                        out[of] = j;
+                    else
+                        set_status(status, DMA_ERR_DEVICE_CHECK);
+                    ++of;
+                } else {
+                    if (op < kTilePartialCap)
+                        part_s[op] = j;
+                    else
+                        set_status(status, DMA_ERR_DEVICE_CHECK);
+                    ++op;
+                }
+            }
+            if (bitmap) {
+                for (int b64 = u0[i] / kBitmapBlock; b64 <= (u0[i] + c - 1) / kBitmapBlock; ++b64)
+                    atomicOr(&bm[b64 / 32], 1u << (b64 & 31));
+            }
         }
-        if (act_part) {
-            const int o = run_part + before_part;
-            if (o < kTilePartialCap)
-                part_s[o] = j;
-            else
-                set_status(status, DMA_ERR_DEVICE_CHECK);
-        }
-        if (bitmap && (act_full | act_part)) atomicOr(&bm[j / (kBitmapBlock * 32)], 1u << ((j / kBitmapBlock) & 31));
-        run_full += tot_full;
-        run_part += tot_part;
-        __syncthreads();
-        if (stop) break;
+        run_full += tot.x;
+        run_part += tot.y;
     }
+    __syncthreads();  // part_s complete
     run_part = min(run_part, kTilePartialCap);
     for (int t = threadIdx.x; t < run_part; t += kTileThreads) {
         const int o = run_full + t;
@@ -745,6 +910,11 @@ SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block)
         pl.off_bexp = o;
         o = align_up(o + nu * 4, 256);
     }
+    pl.nlc = (std::max(S, n) + kListChunk - 1) / kListChunk;
+    pl.off_lcnt = o;
+    o = align_up(o + (size_t)pl.nseg * pl.nlc * 16, 256);
+    pl.off_krn = o;
+    o = align_up(o + (size_t)pl.nseg * 4, 256);
     pl.bytes = o;
     return pl;
 }
@@ -812,15 +982,26 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
         expand_block_kernel<<<dim3((S + 255) / 256, nseg), 256, 0, st>>>(bexp, S, n, block, kept->expiry);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // 4. lists
-    compact_kernel<<<nseg, kCompactThreads, 0, st>>>(kept->expiry, S, block, kept->idx, kept->count, kept->top_idx,
-                                                     kept->top_count, kept->top_cap, status);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (kept->tile_idx) {
-        tile_list_kernel<<<dim3(kept->n_qt, nseg), kTileThreads, kept->bitmap ? kept->bitmap_words * 4 : 0, st>>>(
-            kept->expiry, kept->idx, kept->count, S, block, kept->window, kept->n_qt, kept->tile_stride,
-            kept->bitmap_words, kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
+    // 4. lists: the ever-kept keys and the last row's top set (index order), the ever-kept units
+    // in rank order (into the sort's key buffers, free by now), then the per-tile key lists
+    {
+        int4* lcnt = reinterpret_cast<int4*>(W + pl.off_lcnt);
+        int32_t* kr_u = reinterpret_cast<int32_t*>(keyb[0]);
+        int32_t* kr_e = reinterpret_cast<int32_t*>(keyb[1]);
+        int32_t* kr_n = reinterpret_cast<int32_t*>(W + pl.off_krn);
+        const int32_t* p = valb[1];
+        dim3 grid(pl.nlc, nseg);
+        list_count_kernel<<<grid, kListThreads, 0, st>>>(kept->expiry, p, S, n, block, pl.nlc, lcnt, status);
+        list_write_kernel<<<grid, kListThreads, 0, st>>>(kept->expiry, p, S, n, block, pl.nlc, lcnt, kept->idx,
+                                                         kept->count, kept->top_idx, kept->top_count, kept->top_cap,
+                                                         kr_u, kr_e, kr_n, status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (kept->tile_idx) {
+            tile_list_kernel<<<dim3(kept->n_qt, nseg), kTileThreads, kept->bitmap ? kept->bitmap_words * 4 : 0, st>>>(
+                kr_u, kr_e, kr_n, S, n, block, kept->window, kept->n_qt, kept->tile_stride, kept->bitmap_words,
+                kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }

@@ -100,8 +100,10 @@ typedef struct {
     int32_t* tile_idx;    /* [B][Hkv][n_qt][tile_stride]: keys j <= q0 - window (all j <= q1 when
                                             window == 0) whose top interval meets the tile's rows
                                             [q0, q1]: first the keys in the top set of every row of
-                                            the tile, ascending, then the others, ascending; the
-                                            window band (q0-window, q1] is implicit */
+                                            the tile, then the others; each group in rank order
+                                            (score descending, ties to the lower index; block
+                                            units: block rank, then the block's keys ascending);
+                                            the window band (q0-window, q1] is implicit */
     uint32_t* bitmap;     /* [B][Hkv][n_qt][bitmap_words]: bit (tile, 64-key block) set iff some key
                                             of the block is kept by some row of the tile; nullable */
 } dma_kept_t;

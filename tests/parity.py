@@ -105,10 +105,11 @@ def check_expiry(gpu_ex: torch.Tensor, or_ex: torch.Tensor, or_scores: torch.Ten
 
 
 def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 128, tiles=None):
-    """Per (b, h, tile): the gathered key list (keys kept by every row of the
-    tile first, then the keys kept by only some of its rows, each ascending) and
-    the 64-key occupancy bitmap, derived from the oracle's intervals by their
-    definitions."""
+    """Per (b, h, tile): the keys of the gathered list kept by every row of the
+    tile and those kept by only some of its rows (two ascending arrays: the
+    kernel emits each group in rank order, which check_tile_list verifies
+    separately), and the 64-key occupancy bitmap, all derived from the oracle's
+    intervals by their definitions."""
     o = or_ex.cpu().numpy()
     B, Hkv, S = o.shape
     lo = top_lo(S, block)
@@ -125,8 +126,7 @@ def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 1
                 top = (lo <= q1) & (e > q0) & (np.maximum(q0, lo) <= np.minimum(q1, e - 1))
                 sel = top & (j <= lim)
                 every_row = (lo <= q0) & (e > q1)
-                # keys kept by every row of the tile first, then the rest, each ascending
-                lists[(b, h, t)] = np.concatenate([j[sel & every_row], j[sel & ~every_row]])
+                lists[(b, h, t)] = (j[sel & every_row], j[sel & ~every_row])
                 occ = top.copy()
                 if window > 0:
                     occ |= (j <= q1) & (j > q0 - window)
@@ -135,6 +135,36 @@ def expected_tiles(or_ex: torch.Tensor, window: int, block: int, q_tile: int = 1
                 np.bitwise_or.at(bits, blk // 32, (np.uint32(1) << (blk % 32).astype(np.uint32)))
                 bitmaps[(b, h, t)] = bits
     return lists, bitmaps
+
+
+def rank_sort_key(scores32: np.ndarray) -> np.ndarray:
+    """The selection's order as a sortable integer per score: larger is better,
+    -0 equals +0, NaN ranks below every number."""
+    s = np.where(scores32 == 0, np.float32(0), scores32).astype(np.float32)
+    u = s.view(np.uint32).astype(np.int64)
+    neg = (u >> 31) == 1
+    key = np.where(neg, -(u & 0x7FFFFFFF), u)  # monotone in the float value
+    return np.where(np.isnan(s), np.iinfo(np.int64).min, key)
+
+
+def check_tile_list(got: np.ndarray, want_full: np.ndarray, want_part: np.ndarray, gpu_scores32: np.ndarray,
+                    block: int):
+    """A gathered list holds exactly the expected keys, every-row keys first;
+    inside each group the units run best first by the scores the GPU ranked
+    (ties to the lower unit index) and a block's keys ascend."""
+    nf = len(want_full)
+    assert len(got) == nf + len(want_part), (len(got), nf, len(want_part))
+    assert np.array_equal(np.sort(got[:nf]), want_full)
+    assert np.array_equal(np.sort(got[nf:]), want_part)
+    val = rank_sort_key(unit_values(gpu_scores32, block)) if block > 1 else rank_sort_key(gpu_scores32)
+    bs = max(1, block)
+    for part in (got[:nf], got[nf:]):
+        if len(part) < 2:
+            continue
+        a, c = part[:-1], part[1:]
+        ua, uc = a // bs, c // bs
+        ok = (val[a] > val[c]) | ((val[a] == val[c]) & (ua < uc)) | ((ua == uc) & (c == a + 1))
+        assert bool(ok.all()), "tile list out of rank order at %s" % (np.nonzero(~ok)[0][:5],)
 
 
 def check_outputs(O_gpu: torch.Tensor, O_ref: torch.Tensor, lse_gpu, lse_ref, rows, dtype, H: int, Hkv: int,

@@ -56,11 +56,12 @@ def run_prefill_case(dma, inp, w, window, block=1, mode=0, rows=None, tiles=None
         tc = kept.tile_cnt.cpu().numpy()
         ti = kept.tile_idx.cpu().numpy()
         bm = kept.bitmap.cpu().numpy().view(np.uint32)
-        for (b, h, t), want in lists.items():
+        gs = scores.cpu().numpy()
+        for (b, h, t), (want_full, want_part) in lists.items():
             if (b, h) in affected:
                 continue
             got = ti[b, h, t, :tc[b, h, t]]
-            assert np.array_equal(got, want), (b, h, t, got[:8], want[:8])
+            parity.check_tile_list(got, want_full, want_part, gs[b, h], block)
             assert np.array_equal(bm[b, h, t], bitmaps[(b, h, t)]), (b, h, t)
     rows = list(range(S)) if rows is None else rows
     O_ref, lse_ref = oracle.attend_rows(inp["Q"], inp["K"], inp["V"], sc, ex, rows, window, block)
