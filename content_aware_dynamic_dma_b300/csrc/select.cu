@@ -277,17 +277,25 @@ __global__ void count_table_kernel(const int32_t* __restrict__ p, int n, int T, 
     for (int t = threadIdx.x; t < nX; t += blockDim.x) tab[((int64_t)seg * nC + c) * nX + t] = cnt[t];
 }
 
-// In place: tab[seg][c][xb] <- number of ranks < c*T in position block xb.
+// In place: tab[seg][c][xb] <- number of ranks < c*T in position block xb.  One
+// thread per (segment, xb) column; the column's counts are read in batches so
+// that the loads of a batch are in flight together.
+constexpr int kPrefixBatch = 16;
 __global__ void count_prefix_kernel(int32_t* __restrict__ tab, int nC, int nX)
 {
-    const int seg = blockIdx.x;
-    for (int xb = threadIdx.x; xb < nX; xb += blockDim.x) {
-        int32_t run = 0;
-        for (int c = 0; c < nC; ++c) {
-            int64_t o = ((int64_t)seg * nC + c) * nX + xb;
-            int32_t v = tab[o];
-            tab[o] = run;
-            run += v;
+    const int seg = blockIdx.y;
+    const int xb = blockIdx.x * blockDim.x + threadIdx.x;
+    if (xb >= nX) return;
+    int32_t* col = tab + (int64_t)seg * nC * nX + xb;
+    int32_t run = 0;
+    for (int c0 = 0; c0 < nC; c0 += kPrefixBatch) {
+        int32_t v[kPrefixBatch];
+#pragma unroll
+        for (int i = 0; i < kPrefixBatch; ++i) v[i] = c0 + i < nC ? col[(int64_t)(c0 + i) * nX] : 0;
+#pragma unroll
+        for (int i = 0; i < kPrefixBatch; ++i) {
+            if (c0 + i < nC) col[(int64_t)(c0 + i) * nX] = run;
+            run += v[i];
         }
     }
 }
@@ -390,18 +398,36 @@ __global__ void __launch_bounds__(kBoundaryThreads) boundary_kernel(const int32_
 }
 
 // One warp per (segment, rank chunk): E[p[t]] = max(p[t], f(t)).
+// kSmem: the CTA first copies the segment's rank array into shared memory as
+// 16-bit values (n <= 65536), so the downward scans for the staircase's next
+// step read shared memory; every warp of the CTA walks one chunk of the same
+// segment.  Otherwise the scans read rank[] from global memory.
 constexpr int kWalkWarps = 4;
-__global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const int32_t* __restrict__ p,
-                                                               const int32_t* __restrict__ rank,
-                                                               const int32_t* __restrict__ f0, int nseg, int n, int k,
-                                                               int T, int nC, int32_t* __restrict__ E, int* status)
+constexpr int kWalkSmemWarps = 32;
+template <bool kSmem>
+__global__ void walk_kernel(const int32_t* __restrict__ p, const int32_t* __restrict__ rank,
+                            const int32_t* __restrict__ f0, int nseg, int n, int k, int T, int nC,
+                            int32_t* __restrict__ E, int* status)
 {
+    extern __shared__ uint16_t rk16[];  // [n] (kSmem)
     const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kWalkWarps + (threadIdx.x >> 5);
-    if (gw >= nseg * nC) return;
-    const int seg = gw / nC, c = gw % nC;
+    int seg, c;
+    if (kSmem) {
+        seg = blockIdx.y;
+        c = blockIdx.x * kWalkSmemWarps + (threadIdx.x >> 5);
+        const int32_t* rsrc = rank + (int64_t)seg * n;
+        for (int x = threadIdx.x; x < n; x += blockDim.x) rk16[x] = (uint16_t)rsrc[x];
+        __syncthreads();
+        if (c >= nC) return;
+    } else {
+        const int gw = blockIdx.x * kWalkWarps + (threadIdx.x >> 5);
+        if (gw >= nseg * nC) return;
+        seg = gw / nC;
+        c = gw % nC;
+    }
     const int32_t* ps = p + (int64_t)seg * n;
     const int32_t* rs = rank + (int64_t)seg * n;
+    auto rank_at = [&](int pos) -> int { return kSmem ? (int)rk16[pos] : rs[pos]; };
     int32_t* Es = E + (int64_t)seg * n;
     const int t_begin = c * T, t_end = min(n, t_begin + T);
     const int t_start = min(t_end, max(t_begin, k));
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(kWalkWarps * 32) walk_kernel(const int32_t* __
 #pragma unroll
                     for (int s = 0; s < 4; ++s) {
                         int pos = base - s * 32 - lane;
-                        bool flag = pos >= 0 && rs[pos] <= t;
+                        bool flag = pos >= 0 && rank_at(pos) <= t;
                         uint32_t m = __ballot_sync(0xffffffffu, flag);
                         if (found < 0 && m) found = base - s * 32 - (__ffs(m) - 1);
                     }
@@ -674,8 +700,12 @@ __global__ void __launch_bounds__(kListThreads) list_write_kernel(
 // ----------------------------------------------------------- per-tile lists ---
 
 constexpr int kTileThreads = 256;
-constexpr int kTilePer = 8;            // consecutive list entries per thread per sweep
+constexpr int kTileWarps = kTileThreads / 32;
+constexpr int kTileGroup = 8;          // consecutive query tiles per CTA
 constexpr int kTilePartialCap = 1024;  // keys kept by only some rows of a tile (at most ~384 by construction)
+constexpr int kTileOccSmem = 64 * 1024;  // largest shared-memory occupancy array (sequences up to 512K keys)
+constexpr int kTilePartBytes = kTileGroup * kTilePartialCap * 4;
+
 // For query tile [q0, q1]: keys j <= lim (lim = q0 - window, or q1 without a
 // window) with lo_j <= q1 and expiry_j > q0.  The keys kept by every row of the
 // tile (lo_j <= q0 and expiry_j > q1) come first, then the keys kept by only some
@@ -684,64 +714,178 @@ constexpr int kTilePartialCap = 1024;  // keys kept by only some rows of a tile 
 // likely to hold a row's maximum first and finds the blocks that need a per-row
 // mask at the end.  Also the bitmap of 64-key blocks holding a kept key
 // (gathered keys and the window band).
+//
+// A CTA builds the lists of kTileGroup consecutive tiles of one segment.  Each
+// warp owns a contiguous slice of the rank-ordered unit list and walks it twice,
+// 32 entries at a time: once to count its keys per tile, once to write them at
+// its offsets; order within a warp comes from ballots (token units: one key per
+// entry) or warp scans (block units), across warps from one block-wide step.
+template <bool kBlocks>
 __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
     const int32_t* __restrict__ kr_u, const int32_t* __restrict__ kr_e, const int32_t* __restrict__ kr_n, int S,
     int n, int block, int window, int n_qt, int tile_stride, int bitmap_words, int32_t* __restrict__ tile_cnt,
     int32_t* __restrict__ tile_idx, uint32_t* __restrict__ bitmap, int* status)
 {
-    extern __shared__ uint32_t bm[];  // [bitmap_words]
-    __shared__ int2 warp_buf[32];
-    __shared__ int part_s[kTilePartialCap];
-    const int seg = blockIdx.y, tile = blockIdx.x;
-    const int q0 = tile * kQTile, q1 = min(S, q0 + kQTile) - 1;
-    const int lim = window > 0 ? q0 - window : q1;
-    const int bs = block <= 1 ? 1 : block;
+    // one byte per (tile, 64-key block), set by plain stores and packed into the bitmap at the
+    // end; for long sequences (occ_smem false) the bits go straight to the bitmap in global
+    // memory with atomics instead
+    // dynamic shared memory: the partial groups, then the occupancy bytes
+    extern __shared__ __align__(16) unsigned char tl_smem[];
+    auto part_s = reinterpret_cast<int(*)[kTilePartialCap]>(tl_smem);  // [kTileGroup]
+    uint8_t* occ = tl_smem + kTilePartBytes;  // [kTileGroup][bitmap_words * 32] when occ_smem
+    __shared__ int2 warp_cnt[kTileWarps][kTileGroup];
+    const int seg = blockIdx.y, tile0 = blockIdx.x * kTileGroup;
+    const int ntile = min(kTileGroup, n_qt - tile0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = lanemask_lt();
+    const int bs = kBlocks ? block : 1;
     const int32_t* ku = kr_u + (int64_t)seg * n;
     const int32_t* ke = kr_e + (int64_t)seg * n;
     const int m = min(max(kr_n[seg], 0), n);
-    int32_t* out = tile_idx + ((int64_t)seg * n_qt + tile) * tile_stride;
-    if (bitmap)
-        for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bm[t] = 0;
-    __syncthreads();
-    int run_full = 0, run_part = 0;
-    for (int base = 0; base < m; base += kTileThreads * kTilePer) {
-        const int e0 = base + kTilePer * (int)threadIdx.x;
-        int nk[kTilePer];  // keys of the entry in the tile's list (0: none), full in the high bit
-        int u0[kTilePer];
-        int full = 0, part = 0;
+    const int occ_len = bitmap_words * 32;
+    const bool occ_smem = kTileGroup * occ_len <= kTileOccSmem;
+    if (bitmap) {
+        if (occ_smem) {
+            for (int t = threadIdx.x; t < kTileGroup * occ_len; t += kTileThreads) occ[t] = 0;
+        } else {
+            for (int t = threadIdx.x; t < ntile * bitmap_words; t += kTileThreads)
+                bitmap[((int64_t)seg * n_qt + tile0) * bitmap_words + t] = 0;
+            __syncthreads();
+        }
+    }
+    auto mark = [&](int g, int b64) {
+        if (occ_smem)
+            occ[g * occ_len + b64] = 1;
+        else
+            atomicOr(&bitmap[((int64_t)seg * n_qt + tile0 + g) * bitmap_words + b64 / 32], 1u << (b64 & 31));
+    };
+    int tq0[kTileGroup], tq1[kTileGroup], tlim[kTileGroup];
 #pragma unroll
-        for (int i = 0; i < kTilePer; ++i) {
-            nk[i] = 0;
-            u0[i] = 0;
-            const int q = e0 + i;
-            if (q < m) {
-                const int u = ku[q], e = ke[q];
-                const int j0 = u * bs;
-                const int lo = top_lo(j0, block);
-                if (u < 0 || j0 >= S) {
-                    set_status(status, DMA_ERR_DEVICE_CHECK);
-                } else if (lo <= q1 && e > q0 && j0 <= lim) {
-                    const int c = min(bs, lim - j0 + 1);  // the block's keys up to lim
-                    const bool f = lo <= q0 && e > q1;
-                    nk[i] = c | (f ? (1 << 30) : 0);
-                    u0[i] = j0;
-                    if (f)
-                        full += c;
-                    else
-                        part += c;
-                }
+    for (int g = 0; g < kTileGroup; ++g) {
+        const int t = min(tile0 + g, n_qt - 1);
+        tq0[g] = t * kQTile;
+        tq1[g] = min(S, tq0[g] + kQTile) - 1;
+        tlim[g] = window > 0 ? tq0[g] - window : tq1[g];
+    }
+    struct Ent {
+        int j0, lo, e;
+        bool valid;
+    };
+    auto load = [&](int q) -> Ent {
+        Ent x{0, 0, 0, false};
+        if (q < m) {
+            const int u = ku[q];
+            x.e = ke[q];
+            x.j0 = u * bs;
+            if (u < 0 || x.j0 >= S) {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+            } else {
+                x.lo = top_lo(x.j0, block);
+                x.valid = true;
             }
         }
-        int2 tot;
-        const int2 before = block_exclusive_scan2(make_int2(full, part), warp_buf, &tot);
-        int of = run_full + before.x, op = run_part + before.y;
+        return x;
+    };
+    // bit g of `member`: the entry has keys in tile g's list; of `full`: they are kept by every row
+    // of the tile.  Both are contiguous tile ranges: the entry is in the list of tiles ta..tb
+    //   lo_j <= q1(t)   <=>  t >= lo / 128
+    //   j0 <= lim(t)    <=>  t >= ceil((j0 + window) / 128)  (window > 0), t >= j0 / 128 otherwise
+    //   expiry > q0(t)  <=>  t <= (expiry - 1) / 128
+    // and kept by every row of tiles fa..fb within it
+    //   lo_j <= q0(t)   <=>  t >= ceil(lo / 128)
+    //   expiry > q1(t)  <=>  expiry == S  or  t <= expiry / 128 - 1
+    const int last_tile = tile0 + ntile - 1;
+    auto masks = [&](const Ent& x, uint32_t& member, uint32_t& full) {
+        member = 0;
+        full = 0;
+        if (!x.valid || x.e <= 0) return;
+        const int ta = max(x.lo / kQTile, window > 0 ? (x.j0 + window + kQTile - 1) / kQTile : x.j0 / kQTile);
+        const int tb = min(n_qt - 1, (x.e - 1) / kQTile);
+        const int fa = max(ta, (x.lo + kQTile - 1) / kQTile);
+        const int fb = x.e >= S ? tb : min(tb, x.e / kQTile - 1);
+        auto range = [&](int a, int b) -> uint32_t {
+            a = max(a, tile0);
+            b = min(b, last_tile);
+            if (a > b) return 0u;
+            return ((2u << (b - tile0)) - 1u) & ~((1u << (a - tile0)) - 1u);
+        };
+        member = range(ta, tb);
+        full = member & range(fa, fb);
+    };
+    auto nkeys = [&](const Ent& x, int g) -> int { return kBlocks ? min(bs, tlim[g] - x.j0 + 1) : 1; };
+    auto warp_excl = [&](int v, int& total) -> int {  // exclusive prefix over the warp, and its total
+        if (!kBlocks) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, v != 0);
+            total = __popc(bal);
+            return __popc(bal & lt);
+        }
+        int x = v;
 #pragma unroll
-        for (int i = 0; i < kTilePer; ++i) {
-            const int c = nk[i] & ((1 << 30) - 1);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        total = __shfl_sync(0xffffffffu, x, 31);
+        return x - v;
+    };
+    // this warp's slice of the list, in multiples of 32 entries
+    const int per = ((m + kTileWarps - 1) / kTileWarps + 31) / 32 * 32;
+    const int w_begin = min(m, warp * per), w_end = min(m, w_begin + per);
+    // pass 1: this lane's key counts per tile, then the warp's
+    int2 cnt[kTileGroup];
+#pragma unroll
+    for (int g = 0; g < kTileGroup; ++g) cnt[g] = make_int2(0, 0);
+#pragma unroll 4
+    for (int qb = w_begin; qb < w_end; qb += 32) {
+        const Ent x = load(qb + lane < w_end ? qb + lane : m);
+        uint32_t mem, full;
+        masks(x, mem, full);
+        if (mem == 0) continue;
+#pragma unroll
+        for (int g = 0; g < kTileGroup; ++g) {
+            const int c = (mem >> g) & 1u ? nkeys(x, g) : 0;
+            if ((full >> g) & 1u)
+                cnt[g].x += c;
+            else
+                cnt[g].y += c;
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < kTileGroup; ++g) {
+        const int vf = __reduce_add_sync(0xffffffffu, cnt[g].x);
+        const int vp = __reduce_add_sync(0xffffffffu, cnt[g].y);
+        if (lane == 0) warp_cnt[warp][g] = make_int2(vf, vp);
+    }
+    __syncthreads();
+    int2 off[kTileGroup];
+#pragma unroll
+    for (int g = 0; g < kTileGroup; ++g) {
+        off[g] = make_int2(0, 0);
+        for (int w = 0; w < warp; ++w) {
+            off[g].x += warp_cnt[w][g].x;
+            off[g].y += warp_cnt[w][g].y;
+        }
+    }
+    // pass 2: write at the warp's offsets, in entry order
+#pragma unroll 2
+    for (int qb = w_begin; qb < w_end; qb += 32) {
+        const Ent x = load(qb + lane < w_end ? qb + lane : m);
+        uint32_t mem, full;
+        masks(x, mem, full);
+        if (__ballot_sync(0xffffffffu, mem != 0) == 0) continue;
+#pragma unroll
+        for (int g = 0; g < kTileGroup; ++g) {
+            const bool f = (full >> g) & 1u;
+            const int c = (mem >> g) & 1u ? nkeys(x, g) : 0;
+            int tf, tp;
+            int of = off[g].x + warp_excl(f ? c : 0, tf);
+            int op = off[g].y + warp_excl(f ? 0 : c, tp);
+            off[g].x += tf;
+            off[g].y += tp;
             if (c == 0) continue;
-            const bool f = (nk[i] >> 30) != 0;
+            int32_t* out = tile_idx + ((int64_t)seg * n_qt + tile0 + g) * tile_stride;
             for (int q = 0; q < c; ++q) {
-                const int j = u0[i] + q;
+                const int j = x.j0 + q;
                 if (f) {
                     if (of < tile_stride)
                         out[of] = j;
@@ -750,39 +894,52 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
                     ++of;
                 } else {
                     if (op < kTilePartialCap)
-                        part_s[op] = j;
+                        part_s[g][op] = j;
                     else
                         set_status(status, DMA_ERR_DEVICE_CHECK);
                     ++op;
                 }
             }
-            if (bitmap) {
-                for (int b64 = u0[i] / kBitmapBlock; b64 <= (u0[i] + c - 1) / kBitmapBlock; ++b64)
-                    atomicOr(&bm[b64 / 32], 1u << (b64 & 31));
+            if (bitmap)
+                for (int b64 = x.j0 / kBitmapBlock; b64 <= (x.j0 + c - 1) / kBitmapBlock; ++b64) mark(g, b64);
+        }
+    }
+    __syncthreads();  // part_s and occ complete
+#pragma unroll
+    for (int g = 0; g < kTileGroup; ++g) {
+        if (g >= ntile) break;
+        int tot_f = 0, tot_p = 0;
+        for (int w = 0; w < kTileWarps; ++w) {
+            tot_f += warp_cnt[w][g].x;
+            tot_p += warp_cnt[w][g].y;
+        }
+        tot_p = min(tot_p, kTilePartialCap);
+        const int tile = tile0 + g;
+        int32_t* out = tile_idx + ((int64_t)seg * n_qt + tile) * tile_stride;
+        for (int t = threadIdx.x; t < tot_p; t += kTileThreads) {
+            const int o = tot_f + t;
+            if (o < tile_stride)
+                out[o] = part_s[g][t];
+            else
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+        }
+        if (threadIdx.x == 0) tile_cnt[(int64_t)seg * n_qt + tile] = min(tot_f + tot_p, tile_stride);
+        if (bitmap && window > 0) {
+            const int band_lo = max(0, tq0[g] - window + 1);
+            for (int b64 = band_lo / kBitmapBlock + threadIdx.x; b64 <= tq1[g] / kBitmapBlock; b64 += kTileThreads)
+                mark(g, b64);
+        }
+    }
+    if (bitmap && occ_smem) {
+        __syncthreads();
+        // warp w packs words w, w + 8, ... of every tile: lane l holds block 32 * word + l
+        for (int g = 0; g < ntile; ++g) {
+            uint32_t* bo = bitmap + ((int64_t)seg * n_qt + tile0 + g) * bitmap_words;
+            for (int wd = warp; wd < bitmap_words; wd += kTileWarps) {
+                const uint32_t bits = __ballot_sync(0xffffffffu, occ[g * occ_len + 32 * wd + lane] != 0);
+                if (lane == 0) bo[wd] = bits;
             }
         }
-        run_full += tot.x;
-        run_part += tot.y;
-    }
-    __syncthreads();  // part_s complete
-    run_part = min(run_part, kTilePartialCap);
-    for (int t = threadIdx.x; t < run_part; t += kTileThreads) {
-        const int o = run_full + t;
-        if (o < tile_stride)
-            out[o] = part_s[t];
-        else
-            set_status(status, DMA_ERR_DEVICE_CHECK);
-    }
-    if (threadIdx.x == 0) tile_cnt[(int64_t)seg * n_qt + tile] = min(run_full + run_part, tile_stride);
-    if (bitmap) {
-        if (window > 0) {
-            const int band_lo = max(0, q0 - window + 1);
-            for (int b64 = band_lo / kBitmapBlock + threadIdx.x; b64 <= q1 / kBitmapBlock; b64 += kTileThreads)
-                atomicOr(&bm[b64 / 32], 1u << (b64 & 31));
-        }
-        __syncthreads();
-        uint32_t* bo = bitmap + ((int64_t)seg * n_qt + tile) * bitmap_words;
-        for (int t = threadIdx.x; t < bitmap_words; t += kTileThreads) bo[t] = bm[t];
     }
 }
 
@@ -884,7 +1041,9 @@ SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block)
     if (pl.k > pl.n) pl.k = pl.n;
     const int n = pl.n > 0 ? pl.n : 1;
     pl.nchunk = (n + kRadixChunk - 1) / kRadixChunk;
-    pl.T = pl.X = std::max(64, pow2_ceil((n + 127) / 128));
+    // about 256 rank chunks per segment: the chunks right after rank k move the staircase at
+    // nearly every rank, so short chunks keep the longest walk short
+    pl.T = pl.X = std::max(64, pow2_ceil((n + 255) / 256));
     pl.nC = (n + pl.T - 1) / pl.T;
     pl.nX = (n + pl.X - 1) / pl.X;
     const size_t nu = (size_t)pl.nseg * n;
@@ -969,12 +1128,22 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
             global_expiry_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(rank, n, pl.k, E);
         } else {
             count_table_kernel<<<dim3(pl.nC, nseg), 256, pl.nX * 4, st>>>(p, n, pl.T, pl.nC, pl.X, pl.nX, tab);
-            count_prefix_kernel<<<nseg, 128, 0, st>>>(tab, pl.nC, pl.nX);
+            count_prefix_kernel<<<dim3((pl.nX + 127) / 128, nseg), 128, 0, st>>>(tab, pl.nC, pl.nX);
             boundary_kernel<<<dim3(pl.nC, nseg), kBoundaryThreads, pl.nX * 4, st>>>(p, rank, tab, n, pl.k, pl.T,
                                                                                     pl.nC, pl.X, pl.nX, f0, status);
-            const int walkers = nseg * pl.nC;
-            walk_kernel<<<(walkers + kWalkWarps - 1) / kWalkWarps, kWalkWarps * 32, 0, st>>>(p, rank, f0, nseg, n,
-                                                                                            pl.k, pl.T, pl.nC, E, status);
+            if (n <= 65536) {
+                const int smem = n * 2;
+                if (smem > 48 * 1024 &&
+                    (e = cudaFuncSetAttribute(walk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+                        cudaSuccess)
+                    return e;
+                walk_kernel<true><<<dim3((pl.nC + kWalkSmemWarps - 1) / kWalkSmemWarps, nseg), kWalkSmemWarps * 32,
+                                    smem, st>>>(p, rank, f0, nseg, n, pl.k, pl.T, pl.nC, E, status);
+            } else {
+                const int walkers = nseg * pl.nC;
+                walk_kernel<false><<<(walkers + kWalkWarps - 1) / kWalkWarps, kWalkWarps * 32, 0, st>>>(
+                    p, rank, f0, nseg, n, pl.k, pl.T, pl.nC, E, status);
+            }
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -997,7 +1166,13 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
                                                          kr_u, kr_e, kr_n, status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if (kept->tile_idx) {
-            tile_list_kernel<<<dim3(kept->n_qt, nseg), kTileThreads, kept->bitmap ? kept->bitmap_words * 4 : 0, st>>>(
+            const int occ = kTileGroup * kept->bitmap_words * 32;
+            const int smem = kTilePartBytes + ((kept->bitmap && occ <= kTileOccSmem) ? occ : 0);
+            auto kern = block > 1 ? tile_list_kernel<true> : tile_list_kernel<false>;
+            if (smem > 48 * 1024 &&
+                (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+                return e;
+            kern<<<dim3((kept->n_qt + kTileGroup - 1) / kTileGroup, nseg), kTileThreads, smem, st>>>(
                 kr_u, kr_e, kr_n, S, n, block, kept->window, kept->n_qt, kept->tile_stride, kept->bitmap_words,
                 kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
