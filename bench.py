@@ -9,11 +9,16 @@ dma_select_topk (FULL), dma_sparse_attn_prefill -- over the 64K-token workload
 count taken from the selection's output, divided by the whole step's time.
 The decode workload (B=64 sequences, 32K-token caches, keep 2048 plus the last
 64) is measured too and reported under "decode": GB/s of selected K and V rows.
+Every other seeded workload -- the tiny fp32 one, 4K with GQA, 16K, and 64K with
+64-key block selection -- is timed as well and reported under "per_config",
+with FULL selection next to UPDATE for decode.  The rows the CPU baseline
+computes with the fp64 oracle are compared with the timed 64K prefill's output
+in the same run ("parity").
 
 Rules kept here: W >= 3 untimed warm-up steps; inputs larger than L2 (Q, K, V
-and O of one step are 805 MB against a 126 MB L2); CUDA events on the launching
+and O of one step are 1342 MB against a 126 MB L2); CUDA events on the launching
 stream with a synchronize and a barrier on both sides; max over ranks; clocks
-sampled by nvidia-smi during the timed region.
+sampled by nvidia-smi during the timed regions (prefill, per-config and decode).
 
 Multi-GPU: the path shards by independent (batch, KV head) units with no data
 exchange, so N ranks each run the full workload (weak scaling) and value is the
@@ -43,18 +48,18 @@ import dma_workloads as wl  # noqa: E402
 METRIC = "prefill eff. TFLOP/s on kept pairs @64K; decode selected-KV GB/s (% of peak)"
 PREFILL_WL = "prefill_s64k_bf16"
 DECODE_WL = "decode_b64_l32k_bf16"
-LAUNCHES_SELECT_TOKEN = 19  # 4 x (hist, scan, scatter) + rank + table + prefix + boundary + walk + compact + tiles
+# launches of one FULL selection: 4 x (hist, scan, scatter) + rank + count table + table
+# prefix + boundary + walk + list count + list write + tile lists; block units add the
+# block maxima and the expansion to keys
+LAUNCHES_SELECT_TOKEN = 21
+LAUNCHES_SELECT_BLOCK_EXTRA = 2
 LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merge
 
 # DRAM bytes (read + write) of one prefill attention launch on the 64K workload, from an ncu
-# capture of that launch itself (metrics dram__bytes_read.sum and dram__bytes_write.sum only, one
-# pass): 939,489,280 bytes read + 522,981,632 bytes written.  The compulsory bytes are 805 MB read
-# (Q 537 MB, K and V 268 MB) and 545 MB written (O 537 MB, lse 8 MB); the extra 134 MB of reads
-# are gathered K/V rows fetched again after leaving L2, and the writes fall short of the
-# compulsory bytes by what is still dirty in L2 when the kernel ends.  Valid only for the kernel
-# source it was taken on: reported as null once that source changes.
-PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 939489280 + 522981632,
-                   "source_sha256": "aa33f5941c9a734a06391d252bafd9817379dbe7ac5ef958efdf045c4e7fd89b"}
+# capture of that launch itself (metrics dram__bytes_read.sum and dram__bytes_write.sum only,
+# one pass).  Valid only for the kernel source it was taken on: reported as null once that
+# source changes.
+PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": None, "source_sha256": None}
 
 
 def load_peaks():
@@ -151,6 +156,8 @@ def max_over_ranks(x: float, world: int) -> float:
 
 def prefill_traffic(workload: str):
     import hashlib
+    if PREFILL_TRAFFIC["bytes"] is None:
+        return None
     src = os.path.join(ROOT, "content_aware_dynamic_dma_b300", "csrc", "prefill_tc.cu")
     try:
         with open(src, "rb") as f:
@@ -177,103 +184,131 @@ def kept_pairs(expiry: torch.Tensor, S: int, window: int, block: int, G: int) ->
     return int((lw + lt - inter).sum().item()) * G
 
 
+def config_keys(cfg, pairs, world=1):
+    """The `config` object of a JSON line: the workload and its sizes (the same keys in both
+    arms)."""
+    return {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "H": cfg.H, "Hkv": cfg.Hkv, "D": cfg.D, "w": cfg.w,
+            "window": cfg.window, "block": cfg.block, "mode": "rowwise", "parallelism": "replicas x%d" % world,
+            "l2": "inputs larger than L2 (Q+K+V+O = %.0f MB per step vs 126 MB)" % (
+                (2 * cfg.B * cfg.S * cfg.H * cfg.D * 2 + 2 * cfg.B * cfg.S * cfg.Hkv * cfg.D * 2) / 1e6),
+            "kept_pairs": pairs, "sparsity_vs_dense_causal": round(1.0 - pairs / (cfg.B * cfg.H * cfg.S *
+                                                                                  (cfg.S + 1) / 2.0), 4)}
+
+
 # --------------------------------------------------------------- prefill ----
 
-def bench_prefill(args, world, rank, peaks, clocks):
-    import content_aware_dynamic_dma_b300 as dma
-    cfg = wl.WORKLOADS[args.workload]
-    inp = wl.make_workload(cfg)
-    dev = torch.device("cuda")
-    Q, K, V = inp["Q"].to(dev), inp["K"].to(dev), inp["V"].to(dev)
-    W = inp["W"].to(dev)
-    A = None
-    B, S, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
-    scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev)
-    kept = dma.Kept(B, Hkv, S, cfg.w, cfg.window, cfg.block, dma.ROWWISE, device=dev)
-    O = torch.empty_like(Q)
-    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
+class Prefill:
+    """Device buffers and the three calls of one prefill step for a workload."""
 
-    def step():
-        dma.dma_score_keys(V, W, A, scores, stream=stream)
-        dma.dma_select_topk(scores, kept, dma.FULL, stream=stream)
-        dma.dma_sparse_attn_prefill(Q, K, V, scores, kept, O, lse, stream=stream)
+    def __init__(self, dma, cfg, inp=None, block=None):
+        self.dma, self.cfg = dma, cfg
+        inp = wl.make_workload(cfg) if inp is None else inp
+        self.inp = inp
+        dev = torch.device("cuda")
+        self.Q, self.K, self.V = inp["Q"].to(dev), inp["K"].to(dev), inp["V"].to(dev)
+        self.W = inp["W"].to(dev)
+        self.A = None if inp["A"] is None else inp["A"].to(dev)
+        self.block = cfg.block if block is None else block
+        B, S, H, Hkv = cfg.B, cfg.S, cfg.H, cfg.Hkv
+        self.scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev)
+        self.kept = dma.Kept(B, Hkv, S, cfg.w, cfg.window, self.block, dma.ROWWISE, device=dev)
+        self.O = torch.empty_like(self.Q)
+        self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+        self.launches = 1 + LAUNCHES_SELECT_TOKEN + (LAUNCHES_SELECT_BLOCK_EXTRA if self.block > 1 else 0) + 1
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert dma.dma_get_device_status() == 0
-    pairs = kept_pairs(kept.expiry, S, cfg.window, cfg.block, H // Hkv)
-    flops = 4.0 * D * pairs
+    def calls(self, stream, ev=None):
+        d = self.dma
+        if ev:
+            ev[0].record(stream)
+        d.dma_score_keys(self.V, self.W, self.A, self.scores, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        d.dma_select_topk(self.scores, self.kept, d.FULL, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        d.dma_sparse_attn_prefill(self.Q, self.K, self.V, self.scores, self.kept, self.O, self.lse, stream=stream)
+        if ev:
+            ev[3].record(stream)
 
-    n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(n):
-        ev[s][0].record(stream)
-        dma.dma_score_keys(V, W, A, scores, stream=stream)
-        ev[s][1].record(stream)
-        dma.dma_select_topk(scores, kept, dma.FULL, stream=stream)
-        ev[s][2].record(stream)
-        dma.dma_sparse_attn_prefill(Q, K, V, scores, kept, O, lse, stream=stream)
-        ev[s][3].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    assert dma.dma_get_device_status() == 0
-    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
-    ms = total_ms / n
-    score_ms = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(n))
-    select_ms = statistics.mean(ev[s][1].elapsed_time(ev[s][2]) for s in range(n))
-    attn_ms = statistics.mean(ev[s][2].elapsed_time(ev[s][3]) for s in range(n))
+    def pairs(self):
+        return kept_pairs(self.kept.expiry, self.cfg.S, self.cfg.window, self.block, self.cfg.H // self.cfg.Hkv)
 
-    # e2e: host (pinned) inputs, copies inside the timed region, read back O
-    e2e = None
-    if not args.no_e2e:
-        hQ, hK, hV = inp["Q"].pin_memory(), inp["K"].pin_memory(), inp["V"].pin_memory()
-        hW = inp["W"].pin_memory()
-        hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hW))
-        d2h = hO.numel() * hO.element_size()
-
-        def e2e_step():
-            Q.copy_(hQ, non_blocking=True)
-            K.copy_(hK, non_blocking=True)
-            V.copy_(hV, non_blocking=True)
-            W.copy_(hW, non_blocking=True)
-            step()
-            hO.copy_(O, non_blocking=True)
-
-        e2e_step()
+    def timed(self, steps, warmup, world=1):
+        """Mean per-kernel times and the whole-step time over `steps` timed steps."""
+        stream = torch.cuda.current_stream()
+        for _ in range(warmup):
+            self.calls(stream)
         torch.cuda.synchronize()
-        ne = max(3, min(n, 5))
+        assert self.dma.dma_get_device_status() == 0
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
         barrier(world)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for s in range(steps):
+            self.calls(stream, ev[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        assert self.dma.dma_get_device_status() == 0
+        total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+        k = [statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(3)]
+        return {"ms": total_ms / steps, "score_ms": k[0], "select_ms": k[1], "attn_ms": k[2]}
+
+    def e2e(self, steps):
+        """The same step with Q, K, V, W copied in from pinned host memory and O copied back
+        every step.  Two device buffer sets let the copies of one step overlap the compute of
+        the step before (host-to-device, compute and device-to-host on three streams)."""
+        d = self.dma
+        hQ, hK, hV = self.inp["Q"].pin_memory(), self.inp["K"].pin_memory(), self.inp["V"].pin_memory()
+        hW = self.inp["W"].pin_memory()
+        hO = [torch.empty(self.O.shape, dtype=self.O.dtype).pin_memory() for _ in range(2)]
+        bufs = [(self.Q, self.K, self.V, self.W, self.O),
+                (torch.empty_like(self.Q), torch.empty_like(self.K), torch.empty_like(self.V),
+                 torch.empty_like(self.W), torch.empty_like(self.O))]
+        h2d_b = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hW))
+        d2h_b = hO[0].numel() * hO[0].element_size()
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        in_done = [torch.cuda.Event() for _ in range(2)]
+        cmp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
+
+        def run(n):
+            for i in range(n):
+                k = i & 1
+                Q, K, V, W, O = bufs[k]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(cmp_done[k])  # step i - 2 is done reading these inputs
+                    Q.copy_(hQ, non_blocking=True)
+                    K.copy_(hK, non_blocking=True)
+                    V.copy_(hV, non_blocking=True)
+                    W.copy_(hW, non_blocking=True)
+                    in_done[k].record(s_in)
+                s_cmp.wait_event(in_done[k])
+                if i >= 2:
+                    s_cmp.wait_event(out_done[k])  # O of step i - 2 has been read back
+                d.dma_score_keys(V, W, self.A, self.scores, stream=s_cmp)
+                d.dma_select_topk(self.scores, self.kept, d.FULL, stream=s_cmp)
+                d.dma_sparse_attn_prefill(Q, K, V, self.scores, self.kept, O, self.lse, stream=s_cmp)
+                cmp_done[k].record(s_cmp)
+                s_out.wait_event(cmp_done[k])
+                with torch.cuda.stream(s_out):
+                    hO[k].copy_(O, non_blocking=True)
+                    out_done[k].record(s_out)
+
+        run(2)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(ne):
-            e2e_step()
-        b.record(stream)
+        a.record(s_in)
+        run(steps)
+        s_in.wait_stream(s_out)
+        b.record(s_in)
         torch.cuda.synchronize()
-        e_ms = max_over_ranks(a.elapsed_time(b), world) / ne
-        e2e = {"value": round(flops * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3),
-               "steps": ne}
-    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
-    res = {
-        "cfg": cfg, "pairs": pairs, "flops": flops, "ms": ms, "score_ms": score_ms, "select_ms": select_ms,
-        "attn_ms": attn_ms, "attn_tflops": attn_tflops, "clocks": clk, "e2e": e2e,
-        "launches": n * (1 + LAUNCHES_SELECT_TOKEN + (2 if cfg.block > 1 else 0) + 1),
-        "sparsity": 1.0 - pairs / (B * H * S * (S + 1) / 2.0),
-    }
-    return res
+        assert d.dma_get_device_status() == 0
+        return a.elapsed_time(b) / steps, h2d_b, d2h_b
 
 
 # ---------------------------------------------------------------- decode ----
@@ -290,11 +325,25 @@ def bench_decode(args, world):
     d = wl.make_workload(cfg, n_queries=nq, device="cuda")
     st = dma.DecodeState(B, L, H, Hkv, D, cfg.w, cfg.window)
     L0 = L - nq
+    stream = torch.cuda.current_stream()
+    # FULL selection over the score cache (the decode set-up, and c5's FULL figure)
     st.full_select(d["Kc"], d["Vc"], d["W"], length=L0)
+    full = dma.Kept(B, Hkv, L0, cfg.w, cfg.window, 1, dma.ROWWISE, tiles=False)
+    sc0 = st.scores[:, :, :L0].contiguous()
+    for _ in range(2):
+        dma.dma_select_topk(sc0, full, dma.FULL, stream=stream)
+    torch.cuda.synchronize()
+    fe = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    fe[0].record(stream)
+    for i in range(3):
+        dma.dma_select_topk(sc0, full, dma.FULL, stream=stream)
+        fe[i + 1].record(stream)
+    torch.cuda.synchronize()
+    full_ms = statistics.median(fe[i].elapsed_time(fe[i + 1]) for i in range(3))
+    del full, sc0
     o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
     lens = [torch.full((B,), L0 + k + 1, dtype=torch.int32, device="cuda") for k in range(nq)]
-    stream = torch.cuda.current_stream()
     j = torch.arange(cfg.w, device="cuda")
 
     def rows_kept(pos):
@@ -330,18 +379,20 @@ def bench_decode(args, world):
     upd_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(n)]
     kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
     gbs = sum(kv_bytes) / (sum(dec_ms) * 1e-3) / 1e9
-    return {"workload": DECODE_WL if cfg.B == wl.WORKLOADS[DECODE_WL].B else "%s_b%d" % (DECODE_WL, cfg.B), "gbs": gbs, "decode_ms": statistics.mean(dec_ms),
-            "score_update_ms": statistics.mean(upd_ms), "step_ms": step_ms,
-            "selected_kv_bytes_per_step": statistics.mean(kv_bytes)}
+    return {"workload": DECODE_WL if cfg.B == wl.WORKLOADS[DECODE_WL].B else "%s_b%d" % (DECODE_WL, cfg.B),
+            "gbs": gbs, "decode_ms": statistics.mean(dec_ms), "score_update_ms": statistics.mean(upd_ms),
+            "step_ms": step_ms, "selected_kv_bytes_per_step": statistics.mean(kv_bytes),
+            "full_select_ms": full_ms, "full_select_keys": B * Hkv * L0}
 
 
 # ----------------------------------------------------------- CPU oracle -----
 
-def oracle_sample(cfg, n_rows: int, seed: int = 0):
+def oracle_sample(cfg, n_rows: int, seed: int = 0, out=None):
     """Times the fp64 oracle on the host: full score + full select, then dense
     masked attention on n_rows sampled rows of every (b, query head); the
     attention time is scaled to all S rows.  Returns (TFLOP/s on kept pairs,
-    seconds spent, description, threads)."""
+    seconds spent, description, threads, kept pairs); with `out` a dict, also
+    leaves the sampled rows and the oracle's results there."""
     import oracle
     inp = wl.make_workload(cfg)
     t0 = time.perf_counter()
@@ -350,15 +401,17 @@ def oracle_sample(cfg, n_rows: int, seed: int = 0):
     ex = oracle.select(sc, cfg.w, cfg.block)
     t2 = time.perf_counter()
     rows = wl.sample_rows(cfg.S, n_rows, cfg.seed + seed, cfg.w)
-    oracle.attend_rows(inp["Q"], inp["K"], inp["V"], sc, ex, rows, cfg.window, cfg.block)
+    O_ref, lse_ref = oracle.attend_rows(inp["Q"], inp["K"], inp["V"], sc, ex, rows, cfg.window, cfg.block)
     t3 = time.perf_counter()
+    if out is not None:
+        out.update(rows=rows, O_ref=O_ref, lse_ref=lse_ref, expiry=ex)
     pairs = kept_pairs(ex, cfg.S, cfg.window, cfg.block, cfg.H // cfg.Hkv)
     est = (t1 - t0) + (t2 - t1) + (t3 - t2) * cfg.S / len(rows)
     value = 4.0 * cfg.D * pairs / est / 1e12
     desc = ("full score (%.2fs) + full select (%.2fs) + dense masked attention on %d sampled rows of every "
             "(b, query head) (%.2fs), attention scaled to all %d rows" % (t1 - t0, t2 - t1, len(rows), t3 - t2,
                                                                           cfg.S))
-    return value, t3 - t0, desc, oracle.num_threads()
+    return value, t3 - t0, desc, oracle.num_threads(), pairs
 
 
 def run_reference(args, world, rank):
@@ -366,9 +419,9 @@ def run_reference(args, world, rank):
         return
     cfg = wl.WORKLOADS[args.workload]
     vals, secs = [], []
-    desc, thr = "", 1
+    desc, thr, pairs = "", 1, 0
     for s in range(args.warmup + args.steps):
-        v, t, desc, thr = oracle_sample(cfg, args.ref_rows, seed=s)
+        v, t, desc, thr, pairs = oracle_sample(cfg, args.ref_rows, seed=s)
         if s >= args.warmup:
             vals.append(v)
             secs.append(t)
@@ -376,14 +429,73 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "H": cfg.H, "Hkv": cfg.Hkv, "D": cfg.D,
-                       "w": cfg.w, "window": cfg.window, "block": cfg.block, "mode": "rowwise"},
+            "config": config_keys(cfg, pairs, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ main ----
+
+PER_CONFIG = ["prefill_tiny_s256_fp32", "prefill_s4k_gqa_bf16", "prefill_s16k_bf16", "prefill_s64k_block64_bf16"]
+
+
+def parity_vs_oracle(pf, ref):
+    """The timed 64K prefill against the oracle rows of the CPU-baseline sample: per-key
+    intervals compared exactly; outputs on the sampled rows with the tests' bound (2e-2 on bf16
+    arithmetic plus half a bf16 ulp for the output's rounding), leaving out the rows of a
+    KV-head group whose kept set a near-tie swap changed (a key whose expiry differs)."""
+    cfg = pf.cfg
+    G = cfg.H // cfg.Hkv
+    rows = ref["rows"]
+    ge = pf.kept.expiry.cpu().to(torch.int64)
+    oe = ref["expiry"].to(torch.int64)
+    j = torch.arange(cfg.S)
+    lo = j if pf.block <= 1 else (j // pf.block) * pf.block + pf.block - 1
+    keep = torch.ones((cfg.B, len(rows), cfg.H), dtype=torch.bool)
+    rt = torch.tensor(rows, dtype=torch.int64)
+    n_diff = 0
+    for b in range(cfg.B):
+        for h in range(cfg.Hkv):
+            bad = torch.nonzero(ge[b, h] != oe[b, h]).flatten()
+            n_diff += len(bad)
+            for jj in bad.tolist():
+                a0 = max(int(lo[jj]), int(min(ge[b, h, jj], oe[b, h, jj])))
+                a1 = int(max(ge[b, h, jj], oe[b, h, jj]))
+                hit = (rt >= a0) & (rt < a1)
+                keep[b, hit, h * G:(h + 1) * G] = False
+    g = pf.O.double().cpu()[:, rows]
+    O_ref = ref["O_ref"]
+    _, e = torch.frexp(O_ref.abs())
+    half_ulp = torch.ldexp(torch.ones_like(O_ref), (e - 9).to(torch.int32))
+    err = ((g - O_ref).abs()).amax(dim=-1)
+    ex_half = ((g - O_ref).abs() - half_ulp).amax(dim=-1)
+    lse_err = (pf.lse.double().cpu()[:, :, rows] - ref["lse_ref"]).abs().permute(0, 2, 1)
+    k = keep
+    return {"rows_per_head": len(rows), "expiry_keys_differing": n_diff,
+            "row_heads_left_out_near_ties": int((~k).sum()),
+            "max_abs_err": round(float(err[k].max()), 5), "max_err_less_half_ulp": round(float(ex_half[k].max()), 5),
+            "lse_max_abs_err": round(float(lse_err[k].max()), 6),
+            "ok": bool(float(ex_half[k].max()) <= 2e-2 and float(lse_err[k].max()) <= 2e-2)}
+
+
+def per_config_entry(pf, r, peaks):
+    cfg = pf.cfg
+    pairs = pf.pairs()
+    flops = 4.0 * cfg.D * pairs
+    attn = flops / (r["attn_ms"] * 1e-3) / 1e12
+    ent = {"dtype": "f32" if cfg.dtype == "f32" else "bf16", "B": cfg.B, "S": cfg.S, "H": cfg.H, "Hkv": cfg.Hkv,
+           "D": cfg.D, "w": cfg.w, "window": cfg.window, "block": pf.block, "kept_pairs": pairs,
+           "kernels_ms": {"score": round(r["score_ms"], 4), "select": round(r["select_ms"], 4),
+                          "attention": round(r["attn_ms"], 4)},
+           "step_ms": round(r["ms"], 4), "step_tflops": round(flops / (r["ms"] * 1e-3) / 1e12, 3),
+           "attention_tflops": round(attn, 3)}
+    if cfg.dtype == "f32":
+        ent["roofline"] = "fp32 SIMT path (TF32 would break the 1e-4 bound): no tensor-core peak applies"
+    else:
+        ent["attention_frac_of_bf16_peak"] = round(attn / peaks["bf16_tflops"], 4)
+    return ent
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -400,6 +512,7 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=wl.WORKLOADS[DECODE_WL].B,
                     help="sequences of the decode workload (smaller values serve profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=4096, help="rows per (b, head) in the CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per (b, head) per reference-arm step")
@@ -416,42 +529,67 @@ def main():
     world, rank, local = dist_setup()
     peaks = load_peaks()
     clocks = ClockSampler(local)
+    import content_aware_dynamic_dma_b300 as dma
     if args.no_prefill:
         dec = bench_decode(args, world)
         if rank == 0:
+            dec.pop("last")
             print(json.dumps({"metric": "decode selected-KV GB/s", "value": round(dec["gbs"], 2), "unit": "GB/s",
                               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                               "decode": dec}), flush=True)
         return
-    pf = bench_prefill(args, world, rank, peaks, clocks)
+    cfg = wl.WORKLOADS[args.workload]
+    pf = Prefill(dma, cfg)
+    clocks.start()
+    r = pf.timed(args.steps, args.warmup, world)
+    pairs = pf.pairs()
+    flops = 4.0 * cfg.D * pairs
+    e2e = None
+    if not args.no_e2e:
+        ne = max(3, min(args.steps, 5))
+        e_ms, h2d, d2h = pf.e2e(ne)
+        e_ms = max_over_ranks(e_ms, world)
+        e2e = {"value": round(flops * world / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3), "steps": ne,
+               "overlap": "copies of one step overlap the compute of the step before (two buffer sets, "
+                          "three streams)"}
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            c = wl.WORKLOADS[name]
+            if name == "prefill_s64k_block64_bf16" and cfg.name == PREFILL_WL:
+                p = Prefill(dma, c, inp=pf.inp, block=64)  # the same 64K inputs, 64-key block units
+            else:
+                p = Prefill(dma, c)
+            per_config[name] = per_config_entry(p, p.timed(args.steps, args.warmup, world), peaks)
+            del p
+            torch.cuda.empty_cache()
     dec = None if args.no_decode else bench_decode(args, world)
+    clk = clocks.stop()
 
     if rank != 0:
         return
-    cfg = pf["cfg"]
-    value = pf["flops"] * world / (pf["ms"] * 1e-3) / 1e12
+    value = flops * world / (r["ms"] * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
+    attn_tflops = flops / (r["attn_ms"] * 1e-3) / 1e12
+    launches = args.steps * pf.launches
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(pf["ms"], 4), "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": round(r["ms"], 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "H": cfg.H, "Hkv": cfg.Hkv, "D": cfg.D, "w": cfg.w,
-                   "window": cfg.window, "block": cfg.block, "mode": "rowwise", "parallelism": "replicas x%d" % world,
-                   "l2": "inputs larger than L2 (Q+K+V+O = %.0f MB per step vs 126 MB)" % (
-                       (2 * cfg.B * cfg.S * cfg.H * cfg.D * 2 + 2 * cfg.B * cfg.S * cfg.Hkv * cfg.D * 2) / 1e6),
-                   "kept_pairs": pf["pairs"], "sparsity_vs_dense_causal": round(pf["sparsity"], 4)},
-        "roofline": {"bound": "tensor", "kernel": "dma_sparse_attn_prefill", "achieved": round(pf["attn_tflops"], 3),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(pf["attn_tflops"] / peak, 4),
-                     "frac_of_sustained": round(pf["attn_tflops"] / peaks["bf16_tflops_sustained"], 4)
+        "config": config_keys(cfg, pairs, world),
+        "roofline": {"bound": "tensor", "kernel": "dma_sparse_attn_prefill", "achieved": round(attn_tflops, 3),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(attn_tflops / peak, 4),
+                     "frac_of_sustained": round(attn_tflops / peaks["bf16_tflops_sustained"], 4)
                      if peaks.get("bf16_tflops_sustained") else None,
                      "peak_source": peaks["source"] + " bf16 dense (burst)", "traffic": prefill_traffic(cfg.name),
                      "traffic_unit": "bytes per launch (DRAM read + write)",
                      "algorithmic": "4*D flop per kept (query, key) pair, exact pair count from the selection"},
-        "kernels_ms": {"score": round(pf["score_ms"], 4), "select": round(pf["select_ms"], 4),
-                       "attention": round(pf["attn_ms"], 4)},
-        "e2e": pf["e2e"],
-        "gpu_launches": pf["launches"] + (0 if dec is None else LAUNCHES_PER_DECODE_STEP * args.steps),
-        "clocks": pf["clocks"],
+        "kernels_ms": {"score": round(r["score_ms"], 4), "select": round(r["select_ms"], 4),
+                       "attention": round(r["attn_ms"], 4)},
+        "e2e": e2e,
+        "gpu_launches": launches + (0 if dec is None else LAUNCHES_PER_DECODE_STEP * args.steps),
+        "clocks": clk,
     }
     if dec is not None:
         line["decode"] = {"workload": dec["workload"], "value": round(dec["gbs"], 2), "unit": "GB/s",
@@ -460,10 +598,20 @@ def main():
                           "score_and_update_ms": round(dec["score_update_ms"], 4),
                           "step_ms": round(dec["step_ms"], 4),
                           "selected_kv_bytes_per_step": dec["selected_kv_bytes_per_step"]}
+        per_config[dec["workload"]] = {
+            "update_select_and_score_ms": round(dec["score_update_ms"], 4),
+            "full_select_ms": round(dec["full_select_ms"], 4), "full_select_keys": dec["full_select_keys"],
+            "decode_kernel_ms": round(dec["decode_ms"], 4), "decode_gbs": round(dec["gbs"], 2),
+            "decode_frac_of_hbm": round(dec["gbs"] / peaks["hbm_gbs"], 4)}
+    if per_config:
+        line["per_config"] = per_config
     if not args.no_cpu_baseline and world == 1:
-        v, secs, desc, thr = oracle_sample(cfg, args.cpu_rows)
+        ref = {}
+        v, secs, desc, thr, _ = oracle_sample(cfg, args.cpu_rows, out=ref)
         line["cpu_baseline"] = {"value": round(v, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                                 "sample": desc, "seconds": round(secs, 2)}
+        # the oracle rows of that sample, against the timed run's output
+        line["parity"] = parity_vs_oracle(pf, ref)
     print(json.dumps(line), flush=True)
 
 

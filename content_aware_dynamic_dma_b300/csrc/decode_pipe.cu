@@ -32,6 +32,7 @@ using namespace tc;
 constexpr int kStageKeys = 64;
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
+constexpr int kMaxSplitKeys = 8192;  // longest key list of one split (32 KB of shared memory)
 constexpr int kPipeThreads = kConsumerWarps * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -43,9 +44,9 @@ struct PipeLayout {
     static constexpr int kBias = kStages * kStage;      // [stage][64] f32
     static constexpr int kMerge = 0;  // [warp][16][D + 2] f32, over the stages once the pipeline is drained
     static_assert(kConsumerWarps * 16 * (D + 2) * 4 <= kBias, "merge area must fit in the stages");
-    static constexpr int kJs = kBias + kStages * kStageKeys * 4;  // [kStages + 1][64] key indices
-    static constexpr int kEnd = kJs + (kStages + 1) * kStageKeys * 4;
-    static constexpr int kSmemBytes = kEnd + 1024;
+    static constexpr int kKeys = kBias + kStages * kStageKeys * 4;  // the split's key list (runtime length)
+    // bytes of shared memory for a split of at most `max_keys` keys (1024 of slack for alignment)
+    static constexpr int smem_bytes(int max_keys) { return kKeys + max_keys * 4 + 1024; }
 };
 
 struct PipeArgs {
@@ -144,43 +145,46 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     const int L = a.cache_len ? min(max(a.cache_len[b], 1), a.Lmax) : a.Lmax;
     const int n_top = min(max(a.top_count[seg], 0), a.top_cap);
     const int n_all = n_top + a.window;
-    const int per = ((n_all + a.nsplit - 1) / a.nsplit + kStageKeys - 1) / kStageKeys * kStageKeys;
-    const int u_begin = min(n_all, split * per), u_end = min(n_all, u_begin + per);
-    const int nst = (u_end - u_begin + kStageKeys - 1) / kStageKeys;
+    // the list's stages of 64 keys, shared out evenly: split s takes stages
+    // [s * n / nsplit, (s + 1) * n / nsplit)
+    const int nst_all = (n_all + kStageKeys - 1) / kStageKeys;
+    const int st_begin = (int)((int64_t)split * nst_all / a.nsplit);
+    const int st_end = (int)((int64_t)(split + 1) * nst_all / a.nsplit);
+    const int u_begin = min(n_all, st_begin * kStageKeys), u_end = min(n_all, st_end * kStageKeys);
+    const int nst = st_end - st_begin;
     const int32_t* top = a.top_idx + (int64_t)seg * a.top_cap;
     const float* sc = a.scores + (int64_t)seg * a.Lmax;
     const int64_t row_stride = (int64_t)a.Hkv * D;
     const __nv_bfloat16* Kh = Kc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
     const __nv_bfloat16* Vh = Vc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
 
-    // Key indices: thread u < 64 reads the index of key u of a stage one stage before that
-    // stage's copies are issued and leaves it in a small ring in shared memory; the copies
-    // (chunk `part` of rows r0 + kRowsPerPass * m) read their row indices from there.
-    int* js_ring = reinterpret_cast<int*>(sm + L_::kJs);
+    // Key indices: the whole split's key list is read into shared memory once, before the first
+    // copies (a per-stage index load would put its latency into every stage); the copies (chunk
+    // `part` of rows r0 + kRowsPerPass * m of a stage) read their row indices from there.
+    int* keys_s = reinterpret_cast<int*>(sm + L_::kKeys);
+    const int n_keys = u_end - u_begin;
+    for (int i = threadIdx.x; i < n_keys; i += kPipeThreads)
+        keys_s[i] = list_key(u_begin + i, top, n_top, L, a.window);
     const int part = threadIdx.x % kCPR, r0 = threadIdx.x / kCPR;
-    auto key_of = [&](int st) -> int {
-        const int u = u_begin + st * kStageKeys + (int)threadIdx.x;
-        return (st < nst && threadIdx.x < kStageKeys && u < u_end) ? list_key(u, top, n_top, L, a.window) : -1;
-    };
-    auto put_key = [&](int st, int j) {
-        if (threadIdx.x < kStageKeys) js_ring[(st % (kStages + 1)) * kStageKeys + threadIdx.x] = j;
+    auto key_at = [&](int st, int r) -> int {
+        const int i = st * kStageKeys + r;
+        return i < n_keys ? keys_s[i] : -1;
     };
     auto issue = [&](int st) {
         if (st < nst) {
             const int s = st % kStages;
-            const int* jr = js_ring + (st % (kStages + 1)) * kStageKeys;
             const uint32_t kt = sbase + s * L_::kStage, vt = kt + L_::kTile;
 #pragma unroll
             for (int m = 0; m < kSweeps; ++m) {
                 const int r = r0 + kRowsPerPass * m;
-                const int j = jr[r];
+                const int j = key_at(st, r);
                 const bool ok = j >= 0;
                 const int64_t off = (int64_t)(ok ? j : 0) * row_stride + part * 8;
                 cp_async16(kt + sw_off(r, part), Kh + off, ok);
                 cp_async16(vt + sw_off(r, part), Vh + off, ok);
             }
             if (threadIdx.x < kStageKeys) {
-                const int j = jr[threadIdx.x];
+                const int j = key_at(st, threadIdx.x);
                 float* bd = bias_s + s * kStageKeys + threadIdx.x;
                 if (j >= 0)
                     cp_async4(smem_u32(bd), sc + j);
@@ -214,13 +218,10 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads g, g + 8
     const int kr = 16 * warp;  // this warp's 16 keys of each stage
 
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) put_key(st, key_of(st));
-    __syncthreads();
+    __syncthreads();  // the key list is in shared memory
 #pragma unroll
     for (int st = 0; st < kStages - 1; ++st) issue(st);
     for (int st = 0; st < nst; ++st) {
-        const int jn = key_of(st + kStages);  // in flight while this stage is computed
         cp_async_wait<kStages - 2>();  // this thread's copies of stage st have landed
         __syncthreads();               // everyone's have; everyone is done with stage st - 1
         issue(st + kStages - 1);       // into the slot of stage st - 1
@@ -302,7 +303,6 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
                 mma16816(o[n + 1], pa, b2, b3);
             }
         }
-        put_key(st + kStages, jn);  // read after the next iteration's barrier
     }
     cp_async_wait<0>();
     // every warp is done with the stages before they are reused for the merge
@@ -397,7 +397,9 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     a.window = kept->window;
     a.nsplit = nsplit;
     a.c_log2 = scale * kLog2e;
-    const int smem = PipeLayout<D>::kSmemBytes;
+    // the longest split's key list: ceil(stages / nsplit) stages of 64 keys
+    const int max_stages = std::max(1, (kept->top_cap + kept->window + kStageKeys - 1) / kStageKeys);
+    const int smem = PipeLayout<D>::smem_bytes(((max_stages + nsplit - 1) / nsplit) * kStageKeys);
     cudaError_t e = cudaFuncSetAttribute(decode_pipe_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(
@@ -426,28 +428,20 @@ bool decode_pipe_supported(dma_dtype_t dt, int B, int Lmax, int H, int Hkv, int 
     return dt == DMA_BF16 && (D == 64 || D == 128) && H / Hkv <= 16 && (int64_t)B * Lmax * Hkv < ((int64_t)1 << 31);
 }
 
-// Splits per (sequence, KV head): among the counts that give at least about four
-// waves of resident CTAs (two per SM), the one whose last wave is fullest -- a
-// grid of 5.2 waves leaves four fifths of the machine idle during its last one.
-// Never more than the 64-row chunks of the longest list (the workspace is sized
-// for that many).
+// Splits per (sequence, KV head): the fewest that still give about one and a half
+// waves of resident CTAs (two per SM).  Every CTA pays for reading its key list
+// and for filling and draining its copy pipeline, so fewer, longer CTAs win until
+// the grid gets too short to keep the machine busy: on 64 sequences x 8 KV heads
+// with lists of 33 stages, 1 split took 0.114 ms, 2 splits 0.118 ms, 4 splits
+// 0.120 ms and 6 splits 0.130 ms per step.  Never more than the 64-row stages of
+// the longest list (the workspace is sized for that many).
 int decode_pipe_splits(int B, int Hkv, int top_cap, int window)
 {
     const int max_split = std::max(1, (top_cap + window + 63) / 64);
     const int slots = 2 * 148;
     const int segs = B * Hkv;
-    const int want = std::max(1, (4 * slots + segs - 1) / segs);
-    int best = std::min(max_split, want);
-    double best_eff = 0.0;
-    for (int n = want; n <= std::min(max_split, 3 * want); ++n) {
-        const double waves = (double)segs * n / slots;
-        const double eff = waves / std::ceil(waves);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
-            best = n;
-        }
-    }
-    return best;
+    const int want = std::max(1, (3 * slots + 2 * segs - 1) / (2 * segs));  // ceil(1.5 * slots / segs)
+    return std::min(max_split, want);
 }
 
 cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, int B, int Lmax,
@@ -455,7 +449,10 @@ cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, in
                                const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, int* status,
                                cudaStream_t st)
 {
-    const int nsplit = decode_pipe_splits(B, Hkv, kept->top_cap, kept->window);
+    // splits: the policy's, or more when a split's key list would not fit its shared-memory bound
+    const int max_stages = std::max(1, (kept->top_cap + kept->window + kStageKeys - 1) / kStageKeys);
+    const int nsplit = std::max(decode_pipe_splits(B, Hkv, kept->top_cap, kept->window),
+                                (max_stages * kStageKeys + kMaxSplitKeys - 1) / kMaxSplitKeys);
     if (D == 128)
         return launch_typed<128>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kept, scale, o, lse, ws, nsplit,
                                  status, st);
