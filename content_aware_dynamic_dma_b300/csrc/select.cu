@@ -39,6 +39,7 @@ namespace {
 constexpr int kRadixChunk = 2048;   // units per radix-sort chunk
 constexpr int kRadixThreads = 256;  // 8 warps x 8 rounds x 32 lanes
 constexpr int kRadixBins = 256;
+constexpr int kRadixFuseChunks = 64;  // segments of up to 64 chunks: no separate scan launch
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -177,19 +178,51 @@ __global__ void __launch_bounds__(1024) radix_scan_kernel(uint32_t* __restrict__
 // Stable scatter of one chunk.  Warp w owns units [w*256, w*256+256) of the
 // chunk and walks them in 8 rounds of 32, so (warp, round, lane) is the units'
 // original order; __match_any_sync groups the lanes of one digit in a round.
+// hist: with `counts`, the per-(digit, chunk) counts of radix_hist_kernel, from which each CTA
+// computes its own offsets (digit d of chunk c starts after every key of a smaller digit and
+// the digit-d keys of chunks before c); otherwise the offsets themselves (radix_scan_kernel
+// ran: segments with many chunks).  rank: when non-null (the last pass), rank[value] = the
+// key's place in the sorted order is written as well.
 __global__ void __launch_bounds__(kRadixThreads) radix_scatter_kernel(RadixIn in, int n, int nchunk, int shift,
-                                                                      const uint32_t* __restrict__ offs,
+                                                                      const uint32_t* __restrict__ hist, bool counts,
                                                                       uint32_t* __restrict__ key_out,
-                                                                      int32_t* __restrict__ val_out, int* status)
+                                                                      int32_t* __restrict__ val_out,
+                                                                      int32_t* __restrict__ rank, int* status)
 {
     constexpr int kWarps = kRadixThreads / 32;
     constexpr int kRounds = kRadixChunk / kRadixThreads;
+    static_assert(kRadixThreads == kRadixBins, "one thread per digit");
     __shared__ uint32_t wc[kWarps][kRadixBins];
     __shared__ uint32_t gbase[kRadixBins];
+    __shared__ uint32_t wtot[kWarps];
     const int seg = blockIdx.y, chunk = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int t = threadIdx.x; t < kWarps * kRadixBins; t += kRadixThreads) (&wc[0][0])[t] = 0;
-    gbase[threadIdx.x] = offs[((int64_t)seg * kRadixBins + threadIdx.x) * nchunk + chunk];
+    {
+        const uint32_t* hd = hist + ((int64_t)seg * kRadixBins + threadIdx.x) * nchunk;
+        if (counts) {
+            uint32_t tot = 0, pre = 0;
+            for (int c = 0; c < nchunk; ++c) {
+                const uint32_t v = hd[c];
+                tot += v;
+                pre += c < chunk ? v : 0u;
+            }
+            // exclusive scan of the digit totals (thread = digit)
+            uint32_t x = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) wtot[warp] = x;
+            __syncthreads();
+            uint32_t wb = 0;
+            for (int w = 0; w < warp; ++w) wb += wtot[w];
+            gbase[threadIdx.x] = wb + x - tot + pre;
+        } else {
+            gbase[threadIdx.x] = hd[chunk];
+        }
+    }
     __syncthreads();
 
     const int64_t seg_base = (int64_t)seg * n;
@@ -230,23 +263,17 @@ __global__ void __launch_bounds__(kRadixThreads) radix_scatter_kernel(RadixIn in
             if (dl < (uint32_t)n) {
                 key_out[seg_base + dl] = key[r];
                 val_out[seg_base + dl] = val[r];
+                if (rank) {
+                    if (val[r] >= 0 && val[r] < n)
+                        rank[seg_base + val[r]] = (int32_t)dl;
+                    else
+                        set_status(status, DMA_ERR_DEVICE_CHECK);
+                }
             } else {
                 set_status(status, DMA_ERR_DEVICE_CHECK);
             }
         }
     }
-}
-
-__global__ void rank_kernel(const int32_t* __restrict__ p, int n, int32_t* __restrict__ rank, int* status)
-{
-    const int seg = blockIdx.y;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= n) return;
-    const int x = p[(int64_t)seg * n + t];
-    if (x >= 0 && x < n)
-        rank[(int64_t)seg * n + x] = t;
-    else
-        set_status(status, DMA_ERR_DEVICE_CHECK);
 }
 
 // ------------------------------------------------------------ expiry (global) --
@@ -831,15 +858,40 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
     // this warp's slice of the list, in multiples of 32 entries
     const int per = ((m + kTileWarps - 1) / kTileWarps + 31) / 32 * 32;
     const int w_begin = min(m, warp * per), w_end = min(m, w_begin + per);
-    // pass 1: this lane's key counts per tile, then the warp's
+    // pass 1: this lane's key counts per tile, then the warp's.  Token units have one key per
+    // entry: the eight per-tile counts are byte lanes of one 64-bit word each for the two groups,
+    // a member mask added with its bits spread into bytes (flushed before a byte can overflow).
     int2 cnt[kTileGroup];
 #pragma unroll
     for (int g = 0; g < kTileGroup; ++g) cnt[g] = make_int2(0, 0);
+    uint64_t acc_f = 0, acc_p = 0;
+    int acc_n = 0;
+    auto spread = [](uint32_t m8) -> uint64_t {  // bit g of m8 -> byte g
+        uint64_t r = 0;
+#pragma unroll
+        for (int g = 0; g < kTileGroup; ++g) r |= (uint64_t)((m8 >> g) & 1u) << (8 * g);
+        return r;
+    };
+    auto flush = [&]() {
+#pragma unroll
+        for (int g = 0; g < kTileGroup; ++g) {
+            cnt[g].x += (int)((acc_f >> (8 * g)) & 0xffu);
+            cnt[g].y += (int)((acc_p >> (8 * g)) & 0xffu);
+        }
+        acc_f = acc_p = 0;
+        acc_n = 0;
+    };
 #pragma unroll 4
     for (int qb = w_begin; qb < w_end; qb += 32) {
         const Ent x = load(qb + lane < w_end ? qb + lane : m);
         uint32_t mem, full;
         masks(x, mem, full);
+        if (!kBlocks) {
+            acc_f += spread(full);
+            acc_p += spread(mem & ~full);
+            if (++acc_n == 255) flush();
+            continue;
+        }
         if (mem == 0) continue;
 #pragma unroll
         for (int g = 0; g < kTileGroup; ++g) {
@@ -850,6 +902,7 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
                 cnt[g].y += c;
         }
     }
+    if (!kBlocks) flush();
 #pragma unroll
     for (int g = 0; g < kTileGroup; ++g) {
         const int vf = __reduce_add_sync(0xffffffffu, cnt[g].x);
@@ -1115,14 +1168,16 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
             }
             const int shift = 8 * pass;
             dim3 grid(pl.nchunk, nseg);
+            // few chunks per segment: every scatter CTA sums the counts itself (no scan launch)
+            const bool counts = pl.nchunk <= kRadixFuseChunks;
             radix_hist_kernel<<<grid, kRadixThreads, 0, st>>>(in, n, pl.nchunk, shift, hist);
-            radix_scan_kernel<<<nseg, 1024, 0, st>>>(hist, pl.nchunk);
-            radix_scatter_kernel<<<grid, kRadixThreads, 0, st>>>(in, n, pl.nchunk, shift, hist, keyb[pass & 1],
-                                                                 valb[pass & 1], status);
+            if (!counts) radix_scan_kernel<<<nseg, 1024, 0, st>>>(hist, pl.nchunk);
+            radix_scatter_kernel<<<grid, kRadixThreads, 0, st>>>(in, n, pl.nchunk, shift, hist, counts,
+                                                                 keyb[pass & 1], valb[pass & 1],
+                                                                 pass == 3 ? rank : nullptr, status);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         const int32_t* p = valb[1];
-        rank_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(p, n, rank, status);
         // 2-3. unit expiry
         if (kept->mode == DMA_SEL_GLOBAL) {
             global_expiry_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(rank, n, pl.k, E);
