@@ -48,10 +48,10 @@ import dma_workloads as wl  # noqa: E402
 METRIC = "prefill eff. TFLOP/s on kept pairs @64K; decode selected-KV GB/s (% of peak)"
 PREFILL_WL = "prefill_s64k_bf16"
 DECODE_WL = "decode_b64_l32k_bf16"
-# launches of one FULL selection: 4 x (hist, scan, scatter) + rank + count table + table
-# prefix + boundary + walk + list count + list write + tile lists; block units add the
-# block maxima and the expansion to keys
-LAUNCHES_SELECT_TOKEN = 21
+# launches of one FULL selection: 4 x (histogram, scatter) + count table + table prefix +
+# boundary + walk + list count + list write + tile lists; block units add the block maxima and
+# the expansion to keys
+LAUNCHES_SELECT_TOKEN = 15
 LAUNCHES_SELECT_BLOCK_EXTRA = 2
 LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merge
 

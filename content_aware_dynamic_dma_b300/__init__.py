@@ -309,18 +309,23 @@ class DecodeState:
                               dtype=torch.uint8, device=device)
 
     def full_select(self, Kc, Vc, W, A=None, length: Optional[int] = None, stream=None):
-        """Scores the first ``length`` cache rows and selects the top set of row length-1."""
+        """Scores the first ``length`` cache rows and selects the top set of row length-1.
+
+        Everything runs on ``stream`` (torch's current stream when None), the copies of the
+        prefix selection included."""
         length = self.Lmax if length is None else length
+        stream = torch.cuda.current_stream() if stream is None else stream
         dma_score_keys(Vc, W, A, self.scores, 0, length, stream=stream)
         if length == self.Lmax:
             dma_select_topk(self.scores, self.kept, FULL, stream=stream)
             return
-        sub = Kept(self.B, self.Hkv, length, self.kept.w, self.kept.window, 1, ROWWISE, device=self.scores.device,
-                   tiles=False)
-        sc = self.scores[:, :, :length].contiguous()
-        dma_select_topk(sc, sub, FULL, stream=stream)
-        self.kept.top_idx[:, :, :sub.t.top_cap].copy_(sub.top_idx)
-        self.kept.top_count.copy_(sub.top_count)
+        with torch.cuda.stream(stream):
+            sub = Kept(self.B, self.Hkv, length, self.kept.w, self.kept.window, 1, ROWWISE,
+                       device=self.scores.device, tiles=False)
+            sc = self.scores[:, :, :length].contiguous()
+            dma_select_topk(sc, sub, FULL, stream=stream)
+            self.kept.top_idx[:, :, :sub.t.top_cap].copy_(sub.top_idx)
+            self.kept.top_count.copy_(sub.top_count)
 
     def step(self, q, Kc, Vc, W, cache_len: torch.Tensor, new_pos: int, o, lse=None, A=None, scale: float = 0.0,
              stream=None):

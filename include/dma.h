@@ -199,8 +199,10 @@ dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* V
  *     (4 * B * H * ceil((top_cap + window) / 64) * (D + 2) + 256 bytes), the call
  *     returns DMA_ERR_UNSUPPORTED before launching anything.
  *   - Set-up: the first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress); make that first call before
- *     any stream capture.
+ *     array's device address (cudaGetSymbolAddress) and keeps it for the process;
+ *     make that first call before any stream capture.  A cudaDeviceReset of that
+ *     device discards the array with the context: do not call this entry point on
+ *     the device after such a reset.
  *   - Sharing: all calls on a device use the same array, which keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls that overlap
  *     on the GPU -- on different streams, or from different threads -- race on

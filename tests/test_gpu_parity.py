@@ -368,3 +368,20 @@ def test_decode_varying_cache_len(dma, dt):
     assert float(((o.double().cpu() - o_ref).abs() - parity.out_tol(o_ref, dt)).max()) <= 0
     assert float((lse.double().cpu() - lse_ref).abs().max()) <= parity.TOL[dt]
     assert dma.dma_get_device_status() == 0
+
+
+def test_full_select_on_a_side_stream(dma):
+    """DecodeState.full_select with a prefix length runs every step -- scoring, the prefix's
+    FULL selection and the copies of its top set -- on the stream it is given."""
+    B, L, H, Hkv, D, w, window = 2, 1500, 8, 2, 128, 100, 16
+    d = wl.make_decode(B, L, H, Hkv, D, torch.bfloat16, seed=508, n_queries=1, device="cuda")
+    ref = dma.DecodeState(B, L, H, Hkv, D, w, window)
+    ref.full_select(d["Kc"], d["Vc"], d["W"], length=L - 7)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    st = dma.DecodeState(B, L, H, Hkv, D, w, window)
+    torch.cuda.synchronize()
+    st.full_select(d["Kc"], d["Vc"], d["W"], length=L - 7, stream=side)
+    side.synchronize()
+    assert torch.equal(st.kept.top_count, ref.kept.top_count)
+    assert torch.equal(st.kept.top_idx, ref.kept.top_idx)
