@@ -13,6 +13,9 @@ exactly -- bf16 is a subset of fp32 -- and every result is fp64):
 * ``select(scores, w, ...)``    per-key top-set interval end ("expiry")
 * ``attend_rows(...)``          dense masked softmax attention for listed rows
 * ``decode(...)``               the last row of a cache of length L
+* ``attend_backward(...)``      gradients through the kept pairs (dQ, dK, dV, d score)
+* ``score_backward(...)``       gradients through the score (dV, dW, dA)
+* ``backward(...)``             both, for a whole score -> select -> attend pass
 * ``kept_set(...)``             the kept key set of one row, from an expiry array
 
 Method source: Dynamic Mask Attention summary (lsdiaocha.cn), §四 and §五.
@@ -58,6 +61,9 @@ def _load():
         lib.oracle_select.argtypes = [P, I, I, I, I, I, I, P]
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, P, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P]
+        lib.oracle_attend_backward.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, P, P,
+                                               P]
+        lib.oracle_score_backward.argtypes = [P, P, P, P, I, I, I, I, P, P, P]
         lib.oracle_num_threads.restype = I
         _lib = lib
     return _lib
@@ -148,6 +154,54 @@ def decode(q, Kc, Vc, cache_len, scores, w: int, window: int, block: int = 1, mo
     _load().oracle_decode(_ptr(qq), _ptr(k), _ptr(v), _ptr(cl), _ptr(s), B, Lmax, H, Hkv, D, w, window, block,
                           mode, float(scale), _ptr(o), _ptr(lse))
     return torch.from_numpy(o), torch.from_numpy(lse)
+
+
+def attend_backward(Q, K, V, scores, expiry, dO, window: int, block: int = 1, scale: Optional[float] = None,
+                    segment: Optional[int] = None):
+    """Gradients through the kept pairs of the prefill attention, given dO = dL/dO.
+
+    Returns (dQ [B][S][H][D], dK and dV [B][S][Hkv][D], ds [B][Hkv][S]) in fp64: ds is the
+    gradient of the score (the logits' bias).  With ``segment`` = b * Hkv + h, only that
+    (batch, KV head) segment -- its keys and its G query heads' rows -- is computed (the rest
+    is zero)."""
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    q, k, v, do = _f32(Q), _f32(K), _f32(V), _f32(dO)
+    s = np.ascontiguousarray(scores.to(torch.float64).numpy())
+    e = np.ascontiguousarray(expiry.to(torch.int32).numpy())
+    dQ = np.zeros((B, S, H, D), dtype=np.float64)
+    dK = np.zeros((B, S, Hkv, D), dtype=np.float64)
+    dV = np.zeros((B, S, Hkv, D), dtype=np.float64)
+    ds = np.zeros((B, Hkv, S), dtype=np.float64)
+    _load().oracle_attend_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(e), _ptr(do), B, S, H, Hkv, D, window,
+                                   block, float(scale), -1 if segment is None else int(segment), _ptr(dQ),
+                                   _ptr(dK), _ptr(dV), _ptr(ds))
+    return torch.from_numpy(dQ), torch.from_numpy(dK), torch.from_numpy(dV), torch.from_numpy(ds)
+
+
+def score_backward(V, W, A, ds):
+    """Through s = A_h * softplus(v . w_h): returns (dV from the score [B][S][Hkv][D], dW [Hkv][D],
+    dA [Hkv]) in fp64, given ds = dL/ds [B][Hkv][S]."""
+    B, S, Hkv, D = V.shape
+    v, w = _f32(V), _f32(W)
+    a = None if A is None else _f32(A)
+    g = np.ascontiguousarray(ds.to(torch.float64).numpy())
+    dV = np.zeros((B, S, Hkv, D), dtype=np.float64)
+    dW = np.zeros((Hkv, D), dtype=np.float64)
+    dA = np.zeros((Hkv,), dtype=np.float64)
+    _load().oracle_score_backward(_ptr(v), _ptr(w), _ptr(a), _ptr(g), B, S, Hkv, D, _ptr(dV), _ptr(dW), _ptr(dA))
+    return torch.from_numpy(dV), torch.from_numpy(dW), torch.from_numpy(dA)
+
+
+def backward(Q, K, V, W, A, w: int, window: int, dO, block: int = 1, mode: int = ROWWISE, scale=None):
+    """The whole backward of score -> select -> attend: returns (dQ, dK, dV, dW, dA) in fp64,
+    dV holding both the attention's and the score's part."""
+    sc = score(V, W, A)
+    ex = select(sc, w, block, mode)
+    dQ, dK, dV, ds = attend_backward(Q, K, V, sc, ex, dO, window, block, scale)
+    dV2, dW, dA = score_backward(V, W, A, ds)
+    return dQ, dK, dV + dV2, dW, dA
 
 
 def top_lo(j, block: int):

@@ -368,3 +368,149 @@ void oracle_decode(const float* q, const float* Kc, const float* Vc, const int32
         free(ex);
     }
 }
+
+/* ------------------------------------------------------------- backward -- */
+/*
+ * Gradients of a loss L through the forward above, given dO = dL/dO (DMA
+ * summary §四/§五/§七: the same mask in training and inference, and it is fully
+ * differentiable in the kept positions; the top-k selection itself is piecewise
+ * constant, so no gradient passes through the choice of keys, and a skipped
+ * position -- weight exactly 0 -- receives exactly zero gradient).
+ *
+ * For row i (query head hq of KV head h) with kept set K_i:
+ *   x_ij  = scale * <Q_i, K_j> + s_j          p_ij = softmax_j(x_ij) over K_i
+ *   O_i   = sum_j p_ij V_j
+ *   dP_ij = <dO_i, V_j>                       D_i  = sum_j p_ij dP_ij
+ *   dx_ij = p_ij (dP_ij - D_i)                (softmax backward)
+ *   dQ_i  = scale * sum_j dx_ij K_j
+ *   dK_j += scale * dx_ij Q_i                 dV_j += p_ij dO_i
+ *   ds_j += dx_ij                             (the score is the logit's bias)
+ * summed over the rows and the G query heads of the group for the key-side
+ * terms.
+ *
+ * Layouts as the forward; dQ [B][S][H][D], dK and dV [B][S][Hkv][D], ds
+ * [B][Hkv][S], all fp64 and overwritten for the segments computed (segment
+ * seg = b * Hkv + h; seg_only < 0 means every segment).
+ */
+static void backward_row(const float* q, const float* dO_row, const float* K, const float* V, int64_t kv_stride,
+                         const double* score, const int32_t* expiry, int i, int D, int window, int block,
+                         double scale, double* x_buf, double* dP_buf, double* dq, double* dK, double* dV,
+                         double* ds)
+{
+    /* forward of the row: logits over its kept set, softmax */
+    double m = -INFINITY;
+    for (int j = 0; j <= i; ++j) {
+        if (!is_kept(i, j, expiry[j], window, block)) {
+            x_buf[j] = -INFINITY;
+            continue;
+        }
+        const float* k = K + (int64_t)j * kv_stride;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += (double)q[d] * (double)k[d];
+        x_buf[j] = scale * dot + score[j];
+        if (x_buf[j] > m) m = x_buf[j];
+    }
+    for (int d = 0; d < D; ++d) dq[d] = 0.0;
+    if (m == -INFINITY) return; /* empty kept set: the output is the constant 0 */
+    double sum = 0.0;
+    for (int j = 0; j <= i; ++j)
+        if (x_buf[j] != -INFINITY) sum += exp(x_buf[j] - m);
+    /* p_ij into x_buf, dP_ij into dP_buf, D_i */
+    double Di = 0.0;
+    for (int j = 0; j <= i; ++j) {
+        if (x_buf[j] == -INFINITY) continue;
+        double p = exp(x_buf[j] - m) / sum;
+        x_buf[j] = p;
+        const float* v = V + (int64_t)j * kv_stride;
+        double dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += (double)dO_row[d] * (double)v[d];
+        dP_buf[j] = dp;
+        Di += p * dp;
+    }
+    for (int j = 0; j <= i; ++j) {
+        if (!is_kept(i, j, expiry[j], window, block)) continue;
+        double p = x_buf[j];
+        double dx = p * (dP_buf[j] - Di);
+        const float* k = K + (int64_t)j * kv_stride;
+        for (int d = 0; d < D; ++d) {
+            dq[d] += scale * dx * (double)k[d];
+            dK[(int64_t)j * kv_stride + d] += scale * dx * (double)q[d];
+            dV[(int64_t)j * kv_stride + d] += p * (double)dO_row[d];
+        }
+        ds[j] += dx;
+    }
+}
+
+void oracle_attend_backward(const float* Q, const float* K, const float* V, const double* scores,
+                            const int32_t* expiry, const float* dO, int B, int S, int H, int Hkv, int D, int window,
+                            int block, double scale, int seg_only, double* dQ, double* dK, double* dV, double* ds)
+{
+    int G = H / Hkv;
+    int64_t kv_stride = (int64_t)Hkv * D;
+#pragma omp parallel
+    {
+        double* x_buf = (double*)malloc(sizeof(double) * (size_t)S);
+        double* dP_buf = (double*)malloc(sizeof(double) * (size_t)S);
+        /* one segment per iteration: its key-side sums are written by one thread only */
+#pragma omp for schedule(dynamic, 1)
+        for (int seg = 0; seg < B * Hkv; ++seg) {
+            if (seg_only >= 0 && seg != seg_only) continue;
+            int b = seg / Hkv, h = seg % Hkv;
+            const float* Kh = K + ((int64_t)b * S * Hkv + h) * D;
+            const float* Vh = V + ((int64_t)b * S * Hkv + h) * D;
+            double* dKh = dK + ((int64_t)b * S * Hkv + h) * D;
+            double* dVh = dV + ((int64_t)b * S * Hkv + h) * D;
+            double* dsh = ds + (int64_t)seg * S;
+            const double* sc = scores + (int64_t)seg * S;
+            const int32_t* ex = expiry + (int64_t)seg * S;
+            for (int j = 0; j < S; ++j) {
+                dsh[j] = 0.0;
+                for (int d = 0; d < D; ++d) dKh[(int64_t)j * kv_stride + d] = dVh[(int64_t)j * kv_stride + d] = 0.0;
+            }
+            for (int g = 0; g < G; ++g) {
+                int hq = h * G + g;
+                for (int i = 0; i < S; ++i) {
+                    int64_t qo = (((int64_t)b * S + i) * H + hq) * D;
+                    backward_row(Q + qo, dO + qo, Kh, Vh, kv_stride, sc, ex, i, D, window, block, scale, x_buf,
+                                 dP_buf, dQ + qo, dKh, dVh, dsh);
+                }
+            }
+        }
+        free(x_buf);
+        free(dP_buf);
+    }
+}
+
+/* Through the score s_j = A_h * softplus(u_j), u_j = <V_j, W_h> (DMA summary
+ * §五), given ds = dL/ds:
+ *   dA_h  = sum_j ds_j softplus(u_j)
+ *   du_j  = ds_j A_h sigmoid(u_j)             (softplus' = sigmoid)
+ *   dW_h  = sum_j du_j V_j                    dV_j += du_j W_h
+ * over every batch.  dV_add [B][S][Hkv][D] is added to (the value rows also
+ * feed the attention); dW [Hkv][D] and dA [Hkv] are overwritten. */
+static double sigmoid(double x) { return x >= 0 ? 1.0 / (1.0 + exp(-x)) : exp(x) / (1.0 + exp(x)); }
+
+void oracle_score_backward(const float* V, const float* W, const float* A, const double* ds, int B, int S, int Hkv,
+                           int D, double* dV_add, double* dW, double* dA)
+{
+#pragma omp parallel for schedule(static)
+    for (int h = 0; h < Hkv; ++h) {
+        double a = A ? (double)A[h] : 1.0;
+        double da = 0.0;
+        for (int d = 0; d < D; ++d) dW[h * D + d] = 0.0;
+        for (int b = 0; b < B; ++b)
+            for (int j = 0; j < S; ++j) {
+                const float* v = V + (((int64_t)b * S + j) * Hkv + h) * D;
+                double u = 0.0;
+                for (int d = 0; d < D; ++d) u += (double)v[d] * (double)W[h * D + d];
+                double g = ds[((int64_t)b * Hkv + h) * S + j];
+                da += g * softplus(u);
+                double du = g * a * sigmoid(u);
+                for (int d = 0; d < D; ++d) {
+                    dW[h * D + d] += du * (double)v[d];
+                    dV_add[(((int64_t)b * S + j) * Hkv + h) * D + d] += du * (double)W[h * D + d];
+                }
+            }
+        dA[h] = da;
+    }
+}
