@@ -61,8 +61,8 @@ def _load():
         lib.oracle_select.argtypes = [P, I, I, I, I, I, I, P]
         lib.oracle_attend_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, P, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_double, P, P]
-        lib.oracle_attend_backward.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, P, P,
-                                               P]
+        lib.oracle_attend_backward.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, ctypes.c_double, I, P, I, P,
+                                               I, P, P, P, P]
         lib.oracle_score_backward.argtypes = [P, P, P, P, I, I, I, I, P, P, P]
         lib.oracle_num_threads.restype = I
         _lib = lib
@@ -157,13 +157,14 @@ def decode(q, Kc, Vc, cache_len, scores, w: int, window: int, block: int = 1, mo
 
 
 def attend_backward(Q, K, V, scores, expiry, dO, window: int, block: int = 1, scale: Optional[float] = None,
-                    segment: Optional[int] = None):
+                    segment: Optional[int] = None, rows=None, keys=None):
     """Gradients through the kept pairs of the prefill attention, given dO = dL/dO.
 
     Returns (dQ [B][S][H][D], dK and dV [B][S][Hkv][D], ds [B][Hkv][S]) in fp64: ds is the
     gradient of the score (the logits' bias).  With ``segment`` = b * Hkv + h, only that
-    (batch, KV head) segment -- its keys and its G query heads' rows -- is computed (the rest
-    is zero)."""
+    (batch, KV head) segment -- its keys and its G query heads' rows -- is computed; ``rows``
+    (ascending) limits dQ to those rows and ``keys`` limits dK, dV and ds to those keys.
+    Everything not computed is zero."""
     B, S, H, D = Q.shape
     Hkv = K.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
@@ -174,8 +175,11 @@ def attend_backward(Q, K, V, scores, expiry, dO, window: int, block: int = 1, sc
     dK = np.zeros((B, S, Hkv, D), dtype=np.float64)
     dV = np.zeros((B, S, Hkv, D), dtype=np.float64)
     ds = np.zeros((B, Hkv, S), dtype=np.float64)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    kk = None if keys is None else np.ascontiguousarray(np.asarray(keys, dtype=np.int32))
     _load().oracle_attend_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(e), _ptr(do), B, S, H, Hkv, D, window,
-                                   block, float(scale), -1 if segment is None else int(segment), _ptr(dQ),
+                                   block, float(scale), -1 if segment is None else int(segment), _ptr(r),
+                                   0 if r is None else len(r), _ptr(kk), 0 if kk is None else len(kk), _ptr(dQ),
                                    _ptr(dK), _ptr(dV), _ptr(ds))
     return torch.from_numpy(dQ), torch.from_numpy(dK), torch.from_numpy(dV), torch.from_numpy(ds)
 

@@ -378,107 +378,143 @@ void oracle_decode(const float* q, const float* Kc, const float* Vc, const int32
  * position -- weight exactly 0 -- receives exactly zero gradient).
  *
  * For row i (query head hq of KV head h) with kept set K_i:
- *   x_ij  = scale * <Q_i, K_j> + s_j          p_ij = softmax_j(x_ij) over K_i
- *   O_i   = sum_j p_ij V_j
- *   dP_ij = <dO_i, V_j>                       D_i  = sum_j p_ij dP_ij
+ *   x_ij  = scale * <Q_i, K_j> + s_j          p_ij = exp(x_ij - lse_i) over K_i,
+ *   lse_i = log sum_{j in K_i} exp(x_ij)      (the softmax of the forward)
+ *   dP_ij = <dO_i, V_j>                       D_i  = sum_{j in K_i} p_ij dP_ij
  *   dx_ij = p_ij (dP_ij - D_i)                (softmax backward)
- *   dQ_i  = scale * sum_j dx_ij K_j
- *   dK_j += scale * dx_ij Q_i                 dV_j += p_ij dO_i
- *   ds_j += dx_ij                             (the score is the logit's bias)
- * summed over the rows and the G query heads of the group for the key-side
- * terms.
+ *   dQ_i  = scale * sum_{j in K_i} dx_ij K_j
+ *   dK_j  = scale * sum_{i : j in K_i} dx_ij Q_i
+ *   dV_j  = sum_{i : j in K_i} p_ij dO_i
+ *   ds_j  = sum_{i : j in K_i} dx_ij          (the score is the logit's bias)
+ * where the key-side sums run over the rows of every query head of the group.
+ * Computed in three phases, each a plain loop over independent outputs: the row
+ * statistics (lse_i, D_i) of every row, then dQ row by row, then dK, dV and ds
+ * key by key (each key's sum walks the rows i >= j and keeps those whose kept
+ * set holds j).  Each output is written by one loop iteration, so the result
+ * does not depend on the number of threads.
  *
  * Layouts as the forward; dQ [B][S][H][D], dK and dV [B][S][Hkv][D], ds
- * [B][Hkv][S], all fp64 and overwritten for the segments computed (segment
- * seg = b * Hkv + h; seg_only < 0 means every segment).
+ * [B][Hkv][S], all fp64.  Segment seg = b * Hkv + h; seg_only < 0 means every
+ * segment.  rows (n_rows entries, ascending) limits dQ to those rows and keys
+ * (n_keys) limits dK, dV and ds to those keys; NULL means all.  Outputs not
+ * computed are left as they were.
  */
-static void backward_row(const float* q, const float* dO_row, const float* K, const float* V, int64_t kv_stride,
-                         const double* score, const int32_t* expiry, int i, int D, int window, int block,
-                         double scale, double* x_buf, double* dP_buf, double* dq, double* dK, double* dV,
-                         double* ds)
+static double kept_logit(const float* q, const float* k, double s, int D, double scale)
 {
-    /* forward of the row: logits over its kept set, softmax */
-    double m = -INFINITY;
-    for (int j = 0; j <= i; ++j) {
-        if (!is_kept(i, j, expiry[j], window, block)) {
-            x_buf[j] = -INFINITY;
-            continue;
-        }
-        const float* k = K + (int64_t)j * kv_stride;
-        double dot = 0.0;
-        for (int d = 0; d < D; ++d) dot += (double)q[d] * (double)k[d];
-        x_buf[j] = scale * dot + score[j];
-        if (x_buf[j] > m) m = x_buf[j];
-    }
-    for (int d = 0; d < D; ++d) dq[d] = 0.0;
-    if (m == -INFINITY) return; /* empty kept set: the output is the constant 0 */
-    double sum = 0.0;
-    for (int j = 0; j <= i; ++j)
-        if (x_buf[j] != -INFINITY) sum += exp(x_buf[j] - m);
-    /* p_ij into x_buf, dP_ij into dP_buf, D_i */
-    double Di = 0.0;
-    for (int j = 0; j <= i; ++j) {
-        if (x_buf[j] == -INFINITY) continue;
-        double p = exp(x_buf[j] - m) / sum;
-        x_buf[j] = p;
-        const float* v = V + (int64_t)j * kv_stride;
-        double dp = 0.0;
-        for (int d = 0; d < D; ++d) dp += (double)dO_row[d] * (double)v[d];
-        dP_buf[j] = dp;
-        Di += p * dp;
-    }
-    for (int j = 0; j <= i; ++j) {
-        if (!is_kept(i, j, expiry[j], window, block)) continue;
-        double p = x_buf[j];
-        double dx = p * (dP_buf[j] - Di);
-        const float* k = K + (int64_t)j * kv_stride;
-        for (int d = 0; d < D; ++d) {
-            dq[d] += scale * dx * (double)k[d];
-            dK[(int64_t)j * kv_stride + d] += scale * dx * (double)q[d];
-            dV[(int64_t)j * kv_stride + d] += p * (double)dO_row[d];
-        }
-        ds[j] += dx;
-    }
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += (double)q[d] * (double)k[d];
+    return scale * dot + s;
+}
+
+static double dot_f(const float* a, const float* b, int D)
+{
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += (double)a[d] * (double)b[d];
+    return dot;
 }
 
 void oracle_attend_backward(const float* Q, const float* K, const float* V, const double* scores,
                             const int32_t* expiry, const float* dO, int B, int S, int H, int Hkv, int D, int window,
-                            int block, double scale, int seg_only, double* dQ, double* dK, double* dV, double* ds)
+                            int block, double scale, int seg_only, const int32_t* rows, int n_rows,
+                            const int32_t* keys, int n_keys, double* dQ, double* dK, double* dV, double* ds)
 {
-    int G = H / Hkv;
-    int64_t kv_stride = (int64_t)Hkv * D;
-#pragma omp parallel
-    {
-        double* x_buf = (double*)malloc(sizeof(double) * (size_t)S);
-        double* dP_buf = (double*)malloc(sizeof(double) * (size_t)S);
-        /* one segment per iteration: its key-side sums are written by one thread only */
-#pragma omp for schedule(dynamic, 1)
-        for (int seg = 0; seg < B * Hkv; ++seg) {
-            if (seg_only >= 0 && seg != seg_only) continue;
-            int b = seg / Hkv, h = seg % Hkv;
-            const float* Kh = K + ((int64_t)b * S * Hkv + h) * D;
-            const float* Vh = V + ((int64_t)b * S * Hkv + h) * D;
-            double* dKh = dK + ((int64_t)b * S * Hkv + h) * D;
-            double* dVh = dV + ((int64_t)b * S * Hkv + h) * D;
-            double* dsh = ds + (int64_t)seg * S;
-            const double* sc = scores + (int64_t)seg * S;
-            const int32_t* ex = expiry + (int64_t)seg * S;
-            for (int j = 0; j < S; ++j) {
-                dsh[j] = 0.0;
-                for (int d = 0; d < D; ++d) dKh[(int64_t)j * kv_stride + d] = dVh[(int64_t)j * kv_stride + d] = 0.0;
-            }
-            for (int g = 0; g < G; ++g) {
-                int hq = h * G + g;
-                for (int i = 0; i < S; ++i) {
-                    int64_t qo = (((int64_t)b * S + i) * H + hq) * D;
-                    backward_row(Q + qo, dO + qo, Kh, Vh, kv_stride, sc, ex, i, D, window, block, scale, x_buf,
-                                 dP_buf, dQ + qo, dKh, dVh, dsh);
+    const int G = H / Hkv;
+    const int64_t kv_stride = (int64_t)Hkv * D;
+    const int nseg = B * Hkv;
+    const int nr = rows ? n_rows : S, nk = keys ? n_keys : S;
+    /* row statistics of every row of the selected segments: lse_i and D_i */
+    double* lse = (double*)malloc(sizeof(double) * (size_t)B * H * S);
+    double* Dr = (double*)malloc(sizeof(double) * (size_t)B * H * S);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t t = 0; t < (int64_t)nseg * G * S; ++t) {
+        const int i = (int)(t % S), g = (int)((t / S) % G), seg = (int)(t / ((int64_t)S * G));
+        if (seg_only >= 0 && seg != seg_only) continue;
+        const int b = seg / Hkv, h = seg % Hkv, hq = h * G + g;
+        const int64_t qo = (((int64_t)b * S + i) * H + hq) * D, ro = ((int64_t)b * H + hq) * S + i;
+        const float* Kh = K + ((int64_t)b * S * Hkv + h) * D;
+        const float* Vh = V + ((int64_t)b * S * Hkv + h) * D;
+        const double* sc = scores + (int64_t)seg * S;
+        const int32_t* ex = expiry + (int64_t)seg * S;
+        double m = -INFINITY;
+        for (int j = 0; j <= i; ++j) {
+            if (!is_kept(i, j, ex[j], window, block)) continue;
+            const double x = kept_logit(Q + qo, Kh + (int64_t)j * kv_stride, sc[j], D, scale);
+            if (x > m) m = x;
+        }
+        if (m == -INFINITY) { /* empty kept set: the output is the constant 0 */
+            lse[ro] = -INFINITY;
+            Dr[ro] = 0.0;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j <= i; ++j)
+            if (is_kept(i, j, ex[j], window, block))
+                sum += exp(kept_logit(Q + qo, Kh + (int64_t)j * kv_stride, sc[j], D, scale) - m);
+        const double l = m + log(sum);
+        double Di = 0.0;
+        for (int j = 0; j <= i; ++j) {
+            if (!is_kept(i, j, ex[j], window, block)) continue;
+            const double p = exp(kept_logit(Q + qo, Kh + (int64_t)j * kv_stride, sc[j], D, scale) - l);
+            Di += p * dot_f(dO + qo, Vh + (int64_t)j * kv_stride, D);
+        }
+        lse[ro] = l;
+        Dr[ro] = Di;
+    }
+    /* dQ, row by row */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < (int64_t)nseg * G * nr; ++t) {
+        const int ri = (int)(t % nr), g = (int)((t / nr) % G), seg = (int)(t / ((int64_t)nr * G));
+        if (seg_only >= 0 && seg != seg_only) continue;
+        const int i = rows ? rows[ri] : ri;
+        const int b = seg / Hkv, h = seg % Hkv, hq = h * G + g;
+        const int64_t qo = (((int64_t)b * S + i) * H + hq) * D, ro = ((int64_t)b * H + hq) * S + i;
+        const float* Kh = K + ((int64_t)b * S * Hkv + h) * D;
+        const float* Vh = V + ((int64_t)b * S * Hkv + h) * D;
+        const double* sc = scores + (int64_t)seg * S;
+        const int32_t* ex = expiry + (int64_t)seg * S;
+        double* dq = dQ + qo;
+        for (int d = 0; d < D; ++d) dq[d] = 0.0;
+        if (lse[ro] == -INFINITY) continue;
+        for (int j = 0; j <= i; ++j) {
+            if (!is_kept(i, j, ex[j], window, block)) continue;
+            const float* k = Kh + (int64_t)j * kv_stride;
+            const double p = exp(kept_logit(Q + qo, k, sc[j], D, scale) - lse[ro]);
+            const double dx = p * (dot_f(dO + qo, Vh + (int64_t)j * kv_stride, D) - Dr[ro]);
+            for (int d = 0; d < D; ++d) dq[d] += scale * dx * (double)k[d];
+        }
+    }
+    /* dK, dV and ds, key by key */
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t t = 0; t < (int64_t)nseg * nk; ++t) {
+        const int kj = (int)(t % nk), seg = (int)(t / nk);
+        if (seg_only >= 0 && seg != seg_only) continue;
+        const int j = keys ? keys[kj] : kj;
+        const int b = seg / Hkv, h = seg % Hkv;
+        const int64_t ko = (((int64_t)b * S + j) * Hkv + h) * D;
+        const double* sc = scores + (int64_t)seg * S;
+        const int32_t* ex = expiry + (int64_t)seg * S;
+        double* dk = dK + ko;
+        double* dv = dV + ko;
+        double dsj = 0.0;
+        for (int d = 0; d < D; ++d) dk[d] = dv[d] = 0.0;
+        for (int g = 0; g < G; ++g) {
+            const int hq = h * G + g;
+            for (int i = j; i < S; ++i) {
+                if (!is_kept(i, j, ex[j], window, block)) continue;
+                const int64_t qo = (((int64_t)b * S + i) * H + hq) * D, ro = ((int64_t)b * H + hq) * S + i;
+                const double p = exp(kept_logit(Q + qo, K + ko, sc[j], D, scale) - lse[ro]);
+                const double dx = p * (dot_f(dO + qo, V + ko, D) - Dr[ro]);
+                for (int d = 0; d < D; ++d) {
+                    dk[d] += scale * dx * (double)Q[qo + d];
+                    dv[d] += p * (double)dO[qo + d];
                 }
+                dsj += dx;
             }
         }
-        free(x_buf);
-        free(dP_buf);
+        ds[(int64_t)seg * S + j] = dsj;
     }
+    free(lse);
+    free(Dr);
 }
 
 /* Through the score s_j = A_h * softplus(u_j), u_j = <V_j, W_h> (DMA summary

@@ -232,3 +232,22 @@ def test_backward_single_segment_equals_all(oracle_mod):
     assert torch.equal(one[1][b, :, h], full[1][b, :, h])
     assert torch.equal(one[2][b, :, h], full[2][b, :, h])
     assert torch.equal(one[3][b, h], full[3][b, h])
+
+
+def test_backward_sampled_rows_and_keys_equal_all(oracle_mod):
+    """dQ limited to some rows and dK, dV, ds limited to some keys are those rows' and keys'
+    values of the full computation, bit for bit; everything else is left at zero."""
+    B, S, H, Hkv, D, w, window = 1, 150, 4, 2, 16, 12, 6
+    inp = wl.make_prefill(B, S, H, Hkv, D, torch.float32, seed=991, salient=True)
+    dO = torch.randn(B, S, H, D, generator=torch.Generator().manual_seed(12))
+    sc = oracle_mod.score(inp["V"], inp["W"], None)
+    ex = oracle_mod.select(sc, w)
+    full = oracle_mod.attend_backward(inp["Q"], inp["K"], inp["V"], sc, ex, dO, window)
+    rows, keys = [0, 7, 64, 149], [0, 3, 100, 148, 149]
+    part = oracle_mod.attend_backward(inp["Q"], inp["K"], inp["V"], sc, ex, dO, window, rows=rows, keys=keys)
+    assert torch.equal(part[0][:, rows], full[0][:, rows])
+    assert torch.equal(part[1][:, keys], full[1][:, keys])
+    assert torch.equal(part[2][:, keys], full[2][:, keys])
+    assert torch.equal(part[3][:, :, keys], full[3][:, :, keys])
+    other = [i for i in range(S) if i not in rows]
+    assert float(part[0][:, other].abs().max()) == 0.0
