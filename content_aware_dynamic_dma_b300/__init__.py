@@ -11,9 +11,12 @@ The functions carry the C names:
 * ``dma_select_topk``         causal top-w selection (FULL or UPDATE)
 * ``dma_sparse_attn_prefill`` masked softmax attention over the kept keys
 * ``dma_sparse_attn_decode``  the same for one new query row per sequence
+* ``dma_sparse_attn_prefill_backward``  dQ, dK, dV and ds over the kept pairs
+* ``dma_score_keys_backward``  ds -> dW, dA and the score's share of dV
 
-plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and two
-compositions, ``prefill`` and ``DecodeState``, for the common call sequences.
+plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and three
+compositions, ``prefill``, ``prefill_backward`` and ``DecodeState``, for the
+common call sequences.
 """
 from __future__ import annotations
 
@@ -61,7 +64,8 @@ class KeptT(ctypes.Structure):
 EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_attn_prefill",
             "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_sparse_attn_decode_noalloc",
             "dma_get_device_status", "dma_status_string", "dma_last_error_message", "dma_set_prefill_kernel",
-            "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version")
+            "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version", "dma_backward_workspace_size",
+            "dma_sparse_attn_prefill_backward", "dma_score_keys_backward")
 
 
 def _load_lib():
@@ -86,6 +90,9 @@ def _load_lib():
         "dma_set_wait_limit_ns": [ctypes.c_uint64],
         "dma_set_fault_injection": [I],
         "dma_version": [],
+        "dma_backward_workspace_size": [I, I, I, I, I, ctypes.POINTER(Z)],
+        "dma_sparse_attn_prefill_backward": [P, P, P, I, I, I, I, I, I, P, PK, F, P, P, P, P, P, P, P, P, Z, P],
+        "dma_score_keys_backward": [P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -249,6 +256,46 @@ def dma_sparse_attn_decode_noalloc(q: torch.Tensor, Kc: torch.Tensor, Vc: torch.
                                                _ptr(lse), _stream(stream)))
 
 
+def dma_backward_workspace_size(B: int, S: int, H: int, Hkv: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.dma_backward_workspace_size(B, S, H, Hkv, D, ctypes.byref(n)))
+    return n.value
+
+
+def _bwd_ws(ws, B, S, H, Hkv, D, device):
+    if ws is None:
+        ws = torch.empty((dma_backward_workspace_size(B, S, H, Hkv, D),), dtype=torch.uint8, device=device)
+    return ws
+
+
+def dma_sparse_attn_prefill_backward(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scores: torch.Tensor,
+                                     kept: Kept, O: torch.Tensor, lse: torch.Tensor, dO: torch.Tensor,
+                                     dQ: torch.Tensor, dK: torch.Tensor, dV: torch.Tensor, ds: torch.Tensor,
+                                     scale: float = 0.0, ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dQ [B][S][H][D], dK and dV [B][S][Hkv][D], ds [B][Hkv][S] (all fp32) are written."""
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    for name, t in (("dQ", dQ), ("dK", dK), ("dV", dV), ("ds", ds), ("lse", lse)):
+        if t.dtype != torch.float32:
+            raise TypeError("%s must be float32" % name)
+    ws = _bwd_ws(ws, B, S, H, Hkv, D, Q.device)
+    _check(_lib.dma_sparse_attn_prefill_backward(
+        _ptr(Q), _ptr(K), _ptr(V), _dtype(Q), B, S, H, Hkv, D, _ptr(scores), ctypes.byref(kept.t), float(scale),
+        _ptr(O), _ptr(lse), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ds), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dma_score_keys_backward(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor], ds: torch.Tensor,
+                            dV: torch.Tensor, dW: torch.Tensor, dA: Optional[torch.Tensor] = None,
+                            ws: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Adds the score path's share to dV; writes dW [Hkv][D] and dA [Hkv] (fp32)."""
+    B, S, Hkv, D = V.shape
+    ws = _bwd_ws(ws, B, S, Hkv, Hkv, D, V.device)
+    _check(_lib.dma_score_keys_backward(_ptr(V), _dtype(V), B, S, Hkv, D, _ptr(W), _ptr(A), _ptr(ds), _ptr(dV),
+                                        _ptr(dW), _ptr(dA), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)))
+
+
 def dma_get_device_status(stream=None) -> int:
     v = ctypes.c_int(0)
     _check(_lib.dma_get_device_status(_stream(stream), ctypes.byref(v)))
@@ -256,7 +303,7 @@ def dma_get_device_status(stream=None) -> int:
 
 
 def dma_set_prefill_kernel(which: int) -> int:
-    """0 = automatic (tensor-core kernel for bf16), 1 = SIMT kernel."""
+    """0 = automatic (tensor-core kernels for bf16, forward and backward), 1 = SIMT kernels."""
     return _lib.dma_set_prefill_kernel(which)
 
 
@@ -296,6 +343,25 @@ def prefill(Q, K, V, W, A, w: int, window: int, block: int = 1, mode: int = ROWW
     lse = torch.empty((B, H, S), dtype=torch.float32, device=Q.device) if with_lse else None
     dma_sparse_attn_prefill(Q, K, V, scores, kept, O, lse, scale, stream=stream)
     return O, lse, scores, kept
+
+
+def prefill_backward(Q, K, V, W, A, O, lse, scores, kept: Kept, dO, scale: float = 0.0, stream=None):
+    """Backward of ``prefill`` through the same kept sets: returns (dQ, dK, dV, dW, dA), fp32,
+    with dV holding both the attention's and the score's share (dA is None when A is None)."""
+    B, S, H, D = Q.shape
+    Hkv = K.shape[2]
+    dev = Q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    dQ = torch.empty((B, S, H, D), **f32)
+    dK = torch.empty((B, S, Hkv, D), **f32)
+    dV = torch.empty((B, S, Hkv, D), **f32)
+    ds = torch.empty((B, Hkv, S), **f32)
+    dW = torch.empty((Hkv, D), **f32)
+    dA = torch.empty((Hkv,), **f32) if A is not None else None
+    ws = _bwd_ws(None, B, S, H, Hkv, D, dev)
+    dma_sparse_attn_prefill_backward(Q, K, V, scores, kept, O, lse, dO, dQ, dK, dV, ds, scale, ws, stream)
+    dma_score_keys_backward(V, W, A, ds, dV, dW, dA, ws, stream)
+    return dQ, dK, dV, dW, dA
 
 
 class DecodeState:

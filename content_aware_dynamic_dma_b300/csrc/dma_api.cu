@@ -351,4 +351,94 @@ dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* V
     return ok();
 }
 
+dma_status_t dma_backward_workspace_size(int B, int S, int H, int Hkv, int D, size_t* ws_bytes)
+{
+    if (!ws_bytes) return fail(DMA_ERR_INVALID_ARG, "ws_bytes is NULL");
+    if (B < 1 || S < 1 || H < 1 || Hkv < 1 || H % Hkv != 0)
+        return fail(DMA_ERR_INVALID_ARG, "bad sizes B=%d S=%d H=%d Hkv=%d", B, S, H, Hkv);
+    if (D != 64 && D != 128) return fail(DMA_ERR_UNSUPPORTED, "head dim D=%d (supported: 64, 128)", D);
+    *ws_bytes = backward_ws_bytes(B, S, H, Hkv, D);
+    return ok();
+}
+
+dma_status_t dma_sparse_attn_prefill_backward(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B,
+                                              int S, int H, int Hkv, int D, const float* scores,
+                                              const dma_kept_t* kept, float scale, const void* O, const float* lse,
+                                              const void* dO, float* dQ, float* dK, float* dV, float* ds, void* ws,
+                                              size_t ws_bytes, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (H < 1 || H % Hkv != 0) return fail(DMA_ERR_INVALID_ARG, "H=%d must be a positive multiple of Hkv=%d", H, Hkv);
+    if (!Q || !K || !V || !O || !dO || !scores || !lse || !dQ || !dK || !dV || !ds)
+        return fail(DMA_ERR_INVALID_ARG, "Q, K, V, O, dO, scores, lse, dQ, dK, dV and ds must be non-NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(dQ) ||
+        !aligned16(dK) || !aligned16(dV) || !aligned4(scores) || !aligned4(lse) || !aligned4(ds))
+        return fail(DMA_ERR_INVALID_ARG,
+                    "Q, K, V, O, dO, dQ, dK, dV must be 16-byte aligned; scores, lse, ds 4-byte aligned");
+    if ((s = check_kept_geometry(kept, B, Hkv, S)) != DMA_OK) return s;
+    if (!kept->expiry || !kept->tile_cnt || !kept->tile_idx)
+        return fail(DMA_ERR_INVALID_ARG, "the backward needs kept->expiry, tile_cnt and tile_idx");
+    const size_t need = backward_ws_bytes(B, S, H, Hkv, D);
+    if (!ws || ws_bytes < need)
+        return fail(DMA_ERR_WORKSPACE, "backward workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0,
+                    need);
+    if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
+    int* status = nullptr;
+    if ((s = status_ptr(&status)) != DMA_OK) return s;
+    BwdArgs a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.dO = dO;
+    a.scores = scores;
+    a.lse = lse;
+    a.expiry = kept->expiry;
+    a.tile_cnt = kept->tile_cnt;
+    a.tile_idx = kept->tile_idx;
+    a.dQ = dQ;
+    a.dK = dK;
+    a.dV = dV;
+    a.ds = ds;
+    a.delta = static_cast<float*>(ws);
+    a.status = status;
+    a.B = B;
+    a.S = S;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.n_qt = kept->n_qt;
+    a.tile_stride = kept->tile_stride;
+    a.window = kept->window;
+    a.block = kept->block;
+    a.scale = scale;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool tc = g_prefill_kernel == 0 && bwd_tc_supported(dt, D);
+    cudaError_t e = launch_bwd_prep(a, dt, D, tc, st);
+    if (e == cudaSuccess) e = tc ? launch_bwd_tc(a, D, g_wait_ns.load(), st) : launch_bwd_simt(a, dt, D, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return ok();
+}
+
+dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
+                                     const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                                     size_t ws_bytes, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (!V || !W || !ds || !dV || !dW) return fail(DMA_ERR_INVALID_ARG, "V, W, ds, dV and dW must be non-NULL");
+    if (!aligned16(V) || !aligned16(dV) || !aligned4(W) || !aligned4(ds) || !aligned4(dW) || (A && !aligned4(A)) ||
+        (dA && !aligned4(dA)))
+        return fail(DMA_ERR_INVALID_ARG, "V, dV must be 16-byte aligned; W, A, ds, dW, dA 4-byte aligned");
+    const size_t need = backward_ws_bytes(B, S, Hkv, Hkv, D);
+    if (!ws || ws_bytes < need)
+        return fail(DMA_ERR_WORKSPACE, "score backward workspace of %zu bytes given, %zu needed",
+                    ws ? ws_bytes : (size_t)0, need);
+    if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    cudaError_t e = launch_score_bwd(V, dt, B, S, Hkv, D, W, A, ds, dV, dW, dA, ws, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "score backward launch");
+    return ok();
+}
+
 }  // extern "C"

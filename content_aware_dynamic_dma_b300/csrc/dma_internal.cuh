@@ -88,6 +88,32 @@ cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, in
                                const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, int* status,
                                cudaStream_t st);
 
+// ---- backward ---------------------------------------------------------------
+
+// Arguments of the attention backward kernels (pointers as documented at
+// dma_sparse_attn_prefill_backward; delta = the [B][H][S] fp32 workspace).
+struct BwdArgs {
+    const void *Q, *K, *V, *O, *dO;
+    const float* scores;
+    const float* lse;
+    const int32_t *expiry, *tile_cnt, *tile_idx;
+    float *dQ, *dK, *dV, *ds, *delta;
+    int* status;
+    int B, S, H, Hkv, n_qt, tile_stride, window, block;
+    float scale;
+};
+
+size_t backward_ws_bytes(int B, int S, int H, int Hkv, int D);
+// Delta = <dO, O> per row; with `zero`, also dK = dV = ds = 0 (for the accumulating kernels).
+cudaError_t launch_bwd_prep(const BwdArgs& a, dma_dtype_t dt, int D, bool zero, cudaStream_t st);
+cudaError_t launch_bwd_simt(const BwdArgs& a, dma_dtype_t dt, int D, cudaStream_t st);
+// Tensor-core backward (bf16, D = 64 or 128): dQ, then dK/dV/ds accumulated into zeroed arrays.
+bool bwd_tc_supported(dma_dtype_t dt, int D);
+cudaError_t launch_bwd_tc(const BwdArgs& a, int D, uint64_t wait_ns, cudaStream_t st);
+cudaError_t launch_score_bwd(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
+                             const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                             cudaStream_t st);
+
 size_t decode_ws_bytes(int B, int H, int Hkv, int D, int top_cap, int window);
 cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
                           const int32_t* cache_len, int H, int Hkv, int D, const float* scores,

@@ -137,6 +137,12 @@ def make_decode(B: int, L: int, H: int, Hkv: int, D: int, dtype: torch.dtype, se
     return {"W": W.contiguous().to(device), "A": None, "q": q, "Kc": Kc, "Vc": Vc}
 
 
+def make_grad(shape, dtype: torch.dtype, seed: int) -> torch.Tensor:
+    """A seeded upstream gradient dL/dO ~ N(0, 1) on the CPU, in ``dtype``."""
+    g = torch.Generator().manual_seed(seed * 104729 + 17)
+    return _randn(g, tuple(shape)).to(dtype).contiguous()
+
+
 def make_workload(wl: Workload, n_queries: int = 1, device="cpu", batches=None):
     if wl.decode:
         return make_decode(wl.B, wl.S, wl.H, wl.Hkv, wl.D, wl.torch_dtype, wl.seed, wl.salient, n_queries,

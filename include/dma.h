@@ -14,6 +14,9 @@
  *   dma_select_topk          per-key top-set intervals + per-query-tile key lists
  *   dma_sparse_attn_prefill  masked softmax attention over the kept keys
  *   dma_sparse_attn_decode   the same for one new query row per sequence
+ * and two for the backward pass (training through the same mask):
+ *   dma_sparse_attn_prefill_backward  dQ, dK, dV and ds over the kept pairs
+ *   dma_score_keys_backward           ds -> dW, dA and the score's share of dV
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and frees every buffer; the library never
@@ -213,6 +216,62 @@ dma_status_t dma_sparse_attn_decode_noalloc(const void* q, const void* Kc, const
                                             const float* scores, const dma_kept_t* kept, float scale, void* o,
                                             float* lse, dma_stream_t stream);
 
+/* --------------------------------------------------------------- backward --
+ * DMA summary §四 (gradients flow through the top-k: kept positions get
+ * gradients, masked ones exactly zero), §五 (skipping masked positions is exact
+ * in the backward pass too) and §七 (the same sparsity in training and
+ * inference).  With p_ij the forward's weights over row i's kept set:
+ *   dP_ij = <dO_i, V_j>,  Delta_i = <dO_i, O_i>,  dx_ij = p_ij (dP_ij - Delta_i)
+ *   dQ_i = scale sum_j dx_ij K_j      dK_j = scale sum_i dx_ij Q_i
+ *   dV_j = sum_i p_ij dO_i            ds_j = sum_i dx_ij
+ * (sums over i cover the rows of every query head of the KV head); pairs
+ * outside the kept sets contribute nothing.  Through the score
+ * s_j = A_h softplus(u_j), u_j = <V_j, W_h>:
+ *   dA_h = sum ds_j softplus(u_j)     du_j = ds_j A_h sigmoid(u_j)
+ *   dW_h = sum du_j V_j               dV_j += du_j W_h
+ * The selection itself (top-w and the expiry intervals) is piecewise constant
+ * in the scores and has no gradient of its own.
+ */
+
+/* Workspace bytes of dma_sparse_attn_prefill_backward and dma_score_keys_backward
+ * (one size serves both). */
+dma_status_t dma_backward_workspace_size(int B, int S, int H, int Hkv, int D, size_t* ws_bytes);
+
+/* Gradients of dma_sparse_attn_prefill with respect to Q, K, V and the bias s.
+ *   Q, K, V, dt, B, S, H, Hkv, D, scores, kept, scale
+ *            exactly as given to the forward call (kept: the same selection,
+ *            with expiry, tile_cnt and tile_idx)
+ *   O        device [B][S][H][D] (dtype dt)  the forward's output
+ *   lse      device [B][H][S] fp32           the forward's lse (required)
+ *   dO       device [B][S][H][D] (dtype dt)  dL/dO
+ *   dQ       device [B][S][H][D] fp32        written
+ *   dK, dV   device [B][S][Hkv][D] fp32      written (not accumulated into)
+ *   ds       device [B][Hkv][S] fp32         written: dL/ds
+ *   ws       device workspace of dma_backward_workspace_size bytes, 16-byte aligned
+ * Rows with nothing kept contribute nothing.  The bf16 path rounds p_ij and
+ * dx_ij to bf16 as tensor-core operands and sums dK, dV, ds in fp32 in an order
+ * that depends on scheduling; the fp32 path's sums have a fixed order.  Device
+ * conditions (a bounded wait that ran out) are reported as for the forward. */
+dma_status_t dma_sparse_attn_prefill_backward(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B,
+                                              int S, int H, int Hkv, int D, const float* scores,
+                                              const dma_kept_t* kept, float scale, const void* O, const float* lse,
+                                              const void* dO, float* dQ, float* dK, float* dV, float* ds, void* ws,
+                                              size_t ws_bytes, dma_stream_t stream);
+
+/* Gradients of dma_score_keys, given ds = dL/ds:
+ *   V, dt, B, S, Hkv, D, W, A   as given to dma_score_keys (all S keys)
+ *   ds       device [B][Hkv][S] fp32
+ *   dV       device [B][S][Hkv][D] fp32   du_j W_h is ADDED to it (pass the
+ *            attention backward's dV to get the total)
+ *   dW       device [Hkv][D] fp32         written
+ *   dA       device [Hkv] fp32 or NULL    written when non-NULL (with A NULL:
+ *            the gradient with respect to a gate of 1)
+ *   ws       device workspace of dma_backward_workspace_size bytes
+ * dW and dA are summed in a fixed order (the same bits on every run). */
+dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
+                                     const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                                     size_t ws_bytes, dma_stream_t stream);
+
 /* ------------------------------------------------------------------ misc -- */
 
 /* Synchronises `stream`, returns the device status word (a dma_status_t value,
@@ -224,12 +283,13 @@ const char* dma_status_string(dma_status_t s);
 /* Detail of the last failing call on this host thread ("" if none). */
 const char* dma_last_error_message(void);
 
-/* Selects the prefill kernel: 0 = automatic (tensor-core kernel for bf16 when
- * available), 1 = SIMT kernel always.  Process-wide; returns the old value. */
+/* Selects the prefill kernels, forward and backward: 0 = automatic (tensor-core
+ * kernels for bf16 when available), 1 = SIMT kernels always.  Process-wide;
+ * returns the old value. */
 int dma_set_prefill_kernel(int which);
 
 /* Fault detection (a test aid; no effect on results when left at the defaults).
- * Every wait inside the tensor-core prefill kernel (on an mbarrier that a
+ * Every wait inside the tensor-core prefill kernels (forward and backward) (on an mbarrier that a
  * copy, the tensor core or another warp completes) gives up after a time
  * limit: the kernel then records DMA_ERR_TIMEOUT in the device status word
  * (read by dma_get_device_status), every warp of the CTA leaves its loop, the

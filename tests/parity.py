@@ -11,6 +11,13 @@
   the fp32 result; the bound applies to the arithmetic before that rounding, so
   each bf16 element is also granted half a bf16 ulp of the reference value
   (above |O| = 8 that half ulp alone is 0.031, more than 2e-2).
+* Gradients (the backward) match within TOL[dtype] times the gradient tensor's
+  own scale, max(1, max |reference|): the forward's bound, stated for outputs of
+  magnitude about 1, applied to a tensor whose entries are sums of up to
+  thousands of terms (dK, dV of a long-kept key).  The bf16 path rounds p and
+  dx to bf16 as tensor-core operands (relative 2^-9 each) and the forward's O to
+  bf16 (which enters Delta = <dO, O>), so its errors scale with the tensor's
+  magnitude, not with each entry's.
 """
 from __future__ import annotations
 
@@ -192,3 +199,23 @@ def check_outputs(O_gpu: torch.Tensor, O_ref: torch.Tensor, lse_gpu, lse_ref, ro
         d = torch.where(both_inf | ~kl, torch.zeros_like(lg), (lg - lse_ref).abs())
         assert float(d.max()) <= tol, "max |lse - lse_ref| = %.3g" % float(d.max())
     return int((~keep).sum())
+
+
+def check_grad(name: str, got: torch.Tensor, ref: torch.Tensor, dtype, select=None) -> dict:
+    """Gradient `got` (GPU, fp32) against the fp64 `ref` on the entries `select` (an index or
+    boolean mask over the leading dimensions; None = all).  Returns the statistics."""
+    g = got.double().cpu()
+    r = ref.double()
+    if select is not None:
+        g, r = g[select], r[select]
+    if r.numel() == 0:
+        return dict(name=name, n=0)
+    scale = max(1.0, float(r.abs().max()))
+    err = float((g - r).abs().max())
+    bound = TOL[dtype] * scale
+    rms_ref = float(r.pow(2).mean().sqrt())
+    rel_rms = float((g - r).pow(2).mean().sqrt()) / rms_ref if rms_ref > 0 else 0.0
+    stats = dict(name=name, n=int(r.numel()), max_err=err, bound=bound, scale=scale, rel_rms=rel_rms)
+    assert err <= bound, "%s: max error %.4g > bound %.4g (scale %.4g, rel rms %.3g)" % (name, err, bound, scale,
+                                                                                          rel_rms)
+    return stats
