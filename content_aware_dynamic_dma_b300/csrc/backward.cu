@@ -18,6 +18,13 @@
 //   dA_h += ds_j softplus(u_j),     du_j = ds_j A_h sigmoid(u_j)
 //   dW_h += du_j V_j,               dV_j += du_j W_h
 // p_ij is recomputed as exp(scale <Q_i, K_j> + s_j - lse_i) from the forward's lse.
+// Delta_i has two forms: <dO_i, O_i> from the forward's output (for bf16 that O is
+// rounded, and its error, about 2^-9 |dO_i| |O_i|, is the same for every key of the
+// row), and sum_j p_ij dP_ij summed over the kept pairs by the row-side kernel.  The
+// key-side sums (dK, ds, and through ds dW and dA) add dx over thousands of rows, where a
+// per-row error in Delta would not average out (sum_j ds_j = 0 holds only with the summed
+// form); so the row-side kernel, which needs Delta before it has seen every key, uses
+// the first form and writes the second for the key-side kernel.
 //
 // Key j is kept by row i iff  j <= i < j + window  or  lo_j <= i < expiry_j,
 // and lo_j >= j, so the rows that keep j are [j, j + window) united with
@@ -87,12 +94,14 @@ __device__ __forceinline__ float warp_sum(float v)
 
 // ----------------------------------------------------------------- preparation
 // Delta[b][hq][i] = <dO_i, O_i> (fp32), one group of kCPR lanes per (b, i, hq) row (16 bytes
-// per lane); then, when dK is given, dK, dV and ds are zeroed for the accumulating kernels.
+// per lane); then, when dK is given, dK, dV, ds and delta_x are zeroed for the accumulating
+// kernels.
 template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads) bwd_prep_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                                                                int B, int S, int H, float* __restrict__ delta,
                                                                float4* __restrict__ dK, float4* __restrict__ dV,
-                                                               int64_t n_kv4, float* __restrict__ ds, int64_t n_ds)
+                                                               int64_t n_kv4, float* __restrict__ ds, int64_t n_ds,
+                                                               float* __restrict__ delta_x)
 {
     constexpr int kElem = 16 / sizeof(T);
     constexpr int kCPR = D / kElem;  // lanes per row: 8, 16 or 32
@@ -141,13 +150,15 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_prep_kernel(const T* __restri
             dV[t] = z;
         }
         for (int64_t t = tid; t < n_ds; t += nth) ds[t] = 0.f;
+        for (int64_t t = tid; t < rows; t += nth) delta_x[t] = 0.f;
     }
 }
 
 // ------------------------------------------------------------------ row side
 // dQ_i: one warp per (b, query head, row i).  Each lane takes one key of the tile's list per
-// step (gathered keys, then the window band), tests whether row i keeps it, and forms dx_ij;
-// then the warp accumulates dx_ij K_j, lanes splitting D.
+// step (gathered keys, then the window band) and tests whether row i keeps it.  A first sweep
+// sums Delta_i = sum_j p_ij dP_ij (written for the key-side kernel); the second forms dx_ij and
+// the warp accumulates dx_ij K_j, lanes splitting D.
 template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads) bwd_dq_simt_kernel(const BwdArgs a)
 {
@@ -170,7 +181,6 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_simt_kernel(const BwdArgs 
     }
     __syncwarp();
     const float lse_i = a.lse[((int64_t)b * a.H + hq) * a.S + i];
-    const float dl_i = a.delta[((int64_t)b * a.H + hq) * a.S + i];
     const int tile = i / kQTile;
     const int q0 = tile * kQTile, q1 = min(a.S, q0 + kQTile) - 1;
     const int n_g = min(max(a.tile_cnt[(int64_t)seg * a.n_qt + tile], 0), a.tile_stride);
@@ -183,23 +193,38 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_simt_kernel(const BwdArgs 
     const int64_t kv_stride = (int64_t)a.Hkv * D;
     const T* Kh = Kp + ((int64_t)b * a.S * a.Hkv + h) * D;
     const T* Vh = Vp + ((int64_t)b * a.S * a.Hkv + h) * D;
+    // the key of list position u, or -1 when row i does not keep it
+    auto kept_key = [&](int u) -> int {
+        int j = -1;
+        if (u < n_all) j = u < n_g ? gl[u] : band_lo + (u - n_g);
+        if (j < 0 || j >= a.S || j > i) return -1;  // (out of range: never produced by the selection)
+        const int lo = top_lo(j, a.block);
+        return (i - j < W || (lo <= i && i < ex[j])) ? j : -1;
+    };
+    // pass 1: Delta_i = sum_j p_ij dP_ij over the kept keys
+    float dsum = 0.f;
+    for (int u0 = 0; u0 < n_all; u0 += 32) {
+        const int j = kept_key(u0 + lane);
+        if (j >= 0) {
+            const float qk = dot_row<T, D>(Kh + (int64_t)j * kv_stride, q_s[warp]);
+            const float gv = dot_row<T, D>(Vh + (int64_t)j * kv_stride, g_s[warp]);
+            dsum = fmaf(expf(a.scale * qk + sc[j] - lse_i), gv, dsum);
+        }
+    }
+    const float dl_i = warp_sum(dsum);
+    if (lane == 0) a.delta_x[((int64_t)b * a.H + hq) * a.S + i] = dl_i;
+    // pass 2: dQ_i
     float acc[kDL];
 #pragma unroll
     for (int e = 0; e < kDL; ++e) acc[e] = 0.f;
     for (int u0 = 0; u0 < n_all; u0 += 32) {
-        const int u = u0 + lane;
-        int j = -1;
-        if (u < n_all) j = u < n_g ? gl[u] : band_lo + (u - n_g);
-        if (j < 0 || j >= a.S) j = -1;  // never produced by the selection; skipped rather than read
+        const int j = kept_key(u0 + lane);
         float dx = 0.f;
-        if (j >= 0 && j <= i) {
-            const int lo = top_lo(j, a.block);
-            if (i - j < W || (lo <= i && i < ex[j])) {
-                const float qk = dot_row<T, D>(Kh + (int64_t)j * kv_stride, q_s[warp]);
-                const float gv = dot_row<T, D>(Vh + (int64_t)j * kv_stride, g_s[warp]);
-                const float p = expf(a.scale * qk + sc[j] - lse_i);
-                dx = p * (gv - dl_i);
-            }
+        if (j >= 0) {
+            const float qk = dot_row<T, D>(Kh + (int64_t)j * kv_stride, q_s[warp]);
+            const float gv = dot_row<T, D>(Vh + (int64_t)j * kv_stride, g_s[warp]);
+            const float p = expf(a.scale * qk + sc[j] - lse_i);
+            dx = p * (gv - dl_i);
         }
         for (int l = 0; l < 32; ++l) {
             const float dxl = __shfl_sync(0xffffffffu, dx, l);
@@ -265,7 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkv_simt_kernel(const BwdArgs
                 const float gv = dot_row<T, D>(gp + qrow, v_s[warp]);
                 const int64_t rs = ((int64_t)b * a.H + hq) * a.S + i;
                 p = expf(a.scale * qk + s_j - a.lse[rs]);
-                dx = p * (gv - a.delta[rs]);
+                dx = p * (gv - a.delta_x[rs]);
             }
             dsum += dx;
             for (int l = 0; l < 32; ++l) {
@@ -382,7 +407,7 @@ cudaError_t prep_typed(const BwdArgs& a, bool zero, cudaStream_t st)
     bwd_prep_kernel<T, D><<<(unsigned)std::max<int64_t>(blocks, 1), kBwdThreads, 0, st>>>(
         static_cast<const T*>(a.O), static_cast<const T*>(a.dO), a.B, a.S, a.H, a.delta,
         zero ? reinterpret_cast<float4*>(a.dK) : nullptr, reinterpret_cast<float4*>(a.dV), n_kv4, a.ds,
-        (int64_t)a.B * a.Hkv * a.S);
+        (int64_t)a.B * a.Hkv * a.S, a.delta_x);
     return cudaGetLastError();
 }
 
@@ -417,7 +442,7 @@ cudaError_t score_bwd_typed(const void* V, int B, int S, int Hkv, const float* W
 
 size_t backward_ws_bytes(int B, int S, int H, int Hkv, int D)
 {
-    const size_t delta = (size_t)B * H * S * sizeof(float);
+    const size_t delta = 2 * (size_t)B * H * S * sizeof(float);  // delta and delta_x
     const size_t nchunk = ((size_t)S + kScoreBwdKeys - 1) / kScoreBwdKeys;
     const size_t part = (size_t)B * Hkv * nchunk * (D + 1) * sizeof(float);
     const size_t m = delta > part ? delta : part;

@@ -34,6 +34,12 @@
 // which meet at a small mbarrier before either overwrites columns the other
 // still reads.
 //
+// Delta_i: the row kernel forms dx with <dO_i, O_i> (the forward's output, rounded for
+// bf16) and, from the same p and dP, sums Delta_i = sum_j p_ij dP_ij over the kept pairs
+// (the two column halves of a row add into one zeroed array); the key kernel uses that
+// summed form, so its sums over
+// thousands of rows (dK, ds) carry no per-row error from the rounded O.
+//
 // Every wait is bounded (2 s by default); a wait that runs out sets
 // DMA_ERR_TIMEOUT in the device status word and the CTA winds down.
 #include <cmath>
@@ -484,6 +490,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
             if (lse_l2 == -INFINITY) lse_l2 = INFINITY;  // a row that keeps nothing contributes nothing
             const float dl = valid ? a.delta[rs] : 0.f;
             const f2 nl2 = mk2(-lse_l2, -lse_l2), dl2 = mk2(dl, dl);
+            f2 dsum2 = mk2(0.f, 0.f);  // sum of p dP over this half's keys: the summed form of Delta
             for (int k = 0; k < nblk; ++k) {
                 const int u = gq * nblk + k, ridx = u % kIdxStages;
                 ok = wait_warp(kQBarIdxFull + ridx, (u / kIdxStages) & 1) && wait_warp(kQBarSFull + (u & 1), (u >> 1) & 1);
@@ -538,8 +545,10 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 64; e += 2) {
+                    const f2 p2 = mk2(p[e], p[e + 1]), dp2 = mk2(dp[e], dp[e + 1]);
+                    dsum2 = fma2(p2, dp2, dsum2);
                     float d0, d1;
-                    split2(mul2(mk2(p[e], p[e + 1]), sub2(mk2(dp[e], dp[e + 1]), dl2)), d0, d1);
+                    split2(mul2(p2, sub2(dp2, dl2)), d0, d1);
                     pk[e / 2] = pack_bf16(d0, d1);
                 }
                 tmem_st32(tS + 32 * hh, pk);
@@ -550,6 +559,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
                 if (lane == 0) mbar_arrive(bar(kQBarIdxEmpty + ridx));
             }
             if (!ok) break;
+            if (valid) {
+                float d0, d1;
+                split2(dsum2, d0, d1);
+                atomicAdd(a.delta_x + rs, d0 + d1);  // the two column halves of the row
+            }
             // the pass's dQ: scale * accumulator, fp32
             if (!(ok = wait_warp(kQBarDQDone, gq & 1))) break;
             tc_fence_after();
@@ -610,7 +624,8 @@ struct DkvLayout {
     static constexpr int kQ = 2 * kTile;       // 2 stages
     static constexpr int kdO = 4 * kTile;      // 2 stages
     static constexpr int kRows = 6 * kTile;    // [stage][lse 128 | Delta 128] f32
-    static constexpr int kIdx = kRows + 2 * 2 * kRowsPerTile * 4;
+    static constexpr int kRowsStage = 2 * kRowsPerTile * 4;
+    static constexpr int kIdx = kRows + 2 * kRowsStage;
     static constexpr int kBars = kIdx + kIdxStages * kIdxSlot;
     static constexpr int kMisc = kBars + 8 * kKNumBars;
     static constexpr int kEnd = kMisc + 16;
@@ -698,12 +713,13 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
                 const int64_t off = ((int64_t)g.b * a.S * a.H + hq) * D;
                 cp.rows(sbase + L::kQ + s * L::kTile, g.q0, a.S, static_cast<const __nv_bfloat16*>(a.Q) + off, q_stride);
                 cp.rows(sbase + L::kdO + s * L::kTile, g.q0, a.S, static_cast<const __nv_bfloat16*>(a.dO) + off, q_stride);
-                // lse and Delta of the tile's rows (zero past the end: those columns are masked)
+                // lse and the summed Delta of the tile's rows (zero past the end: those columns are
+                // masked)
                 const int64_t rs = ((int64_t)g.b * a.H + hq) * a.S;
-                const uint32_t rows_s = sbase + L::kRows + s * 2 * kRowsPerTile * 4;
+                const uint32_t rows_s = sbase + L::kRows + s * L::kRowsStage;
                 for (int t = ct; t < 2 * kRowsPerTile; t += kCopyThreads) {
                     const int row = t % kRowsPerTile, i = g.q0 + row;
-                    const float* src = (t < kRowsPerTile ? a.lse : a.delta) + rs + min(i, a.S - 1);
+                    const float* src = (t < kRowsPerTile ? a.lse : a.delta_x) + rs + min(i, a.S - 1);
                     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(rows_s + 4 * t), "l"(src),
                                  "r"(i < a.S ? 4 : 0)
                                  : "memory");
@@ -877,7 +893,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
                 ok = wait_warp(kKBarQFull + (u & 1), (u >> 1) & 1) && wait_warp(kKBarSFull, u & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const float* lse_s = reinterpret_cast<const float*>(sm + L::kRows + (u & 1) * 2 * kRowsPerTile * 4) + 64 * hh;
+                const float* lse_s = reinterpret_cast<const float*>(sm + L::kRows + (u & 1) * L::kRowsStage) + 64 * hh;
                 const float* dl_s = lse_s + kRowsPerTile;
                 float p[64];
                 tmem_ld32f(tm + lane_off + 64 * hh, p);

@@ -403,6 +403,7 @@ dma_status_t dma_sparse_attn_prefill_backward(const void* Q, const void* K, cons
     a.dV = dV;
     a.ds = ds;
     a.delta = static_cast<float*>(ws);
+    a.delta_x = a.delta + (size_t)B * H * S;
     a.status = status;
     a.B = B;
     a.S = S;

@@ -91,13 +91,15 @@ cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, in
 // ---- backward ---------------------------------------------------------------
 
 // Arguments of the attention backward kernels (pointers as documented at
-// dma_sparse_attn_prefill_backward; delta = the [B][H][S] fp32 workspace).
+// dma_sparse_attn_prefill_backward).  Workspace: delta [B][H][S] = <dO_i, O_i> from the
+// forward's (rounded) output; delta_x [B][H][S] = sum_j p_ij dP_ij summed by the row-side
+// kernel over the kept pairs, for the key-side kernel.
 struct BwdArgs {
     const void *Q, *K, *V, *O, *dO;
     const float* scores;
     const float* lse;
     const int32_t *expiry, *tile_cnt, *tile_idx;
-    float *dQ, *dK, *dV, *ds, *delta;
+    float *dQ, *dK, *dV, *ds, *delta, *delta_x;
     int* status;
     int B, S, H, Hkv, n_qt, tile_stride, window, block;
     float scale;
