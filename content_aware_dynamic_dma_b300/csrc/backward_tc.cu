@@ -626,11 +626,13 @@ struct DkvLayout {
     static constexpr int kRows = 6 * kTile;    // [stage][lse 128 | Delta 128] f32
     static constexpr int kRowsStage = 2 * kRowsPerTile * 4;
     static constexpr int kIdx = kRows + 2 * kRowsStage;
-    static constexpr int kBars = kIdx + kIdxStages * kIdxSlot;
+    static constexpr int kXpose = kIdx + kIdxStages * kIdxSlot;  // per flush warp: 32 rows x 32 f32
+    static constexpr int kBars = kXpose + 4 * 32 * 32 * 4;
     static constexpr int kMisc = kBars + 8 * kKNumBars;
     static constexpr int kEnd = kMisc + 16;
     static constexpr int kSmemBytes = kEnd + 1024;
 };
+static_assert(DkvLayout<128>::kSmemBytes <= 227 * 1024, "key kernel shared memory");
 
 // bits [lo, hi) of a 64-bit mask, both clipped to [0, 64]
 __device__ __forceinline__ uint64_t range_mask(int lo, int hi)
@@ -819,6 +821,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
     } else if (warp >= kKvFlush0) {
         // ------------------------------------------------------------------ flush
         // Thread = key lane r: the block's dK (times scale) and dV rows added to global memory.
+        // Each 32-column chunk of the warp's 32 rows is turned around in shared memory so that one
+        // 16-byte reduction instruction covers four rows x 128 contiguous bytes (4 L2 requests,
+        // against 32 when every lane adds to its own row).
         regs_decrease<kRegsOther>();
         const Geom g = tile_geom(a, fresh_ctaid());
         const int nblk = g.nblk;
@@ -826,6 +831,26 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
         const int quarter = warp & 3, r = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sc = a.scale;
+        // [row][8 groups of 4 f32], group q of row x stored at position q ^ (x & 7)
+        float* xb = reinterpret_cast<float*>(sm + L::kXpose) + (warp - kKvFlush0) * 32 * 32;
+        const int64_t seg_row0 = (int64_t)g.b * a.S * a.Hkv + g.h;  // row (b, j, h) = seg_row0 + j * Hkv
+        auto put_row = [&](const float* v, float mul) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(xb + lane * 32 + ((q ^ (lane & 7)) * 4)) =
+                    make_float4(mul * v[4 * q], mul * v[4 * q + 1], mul * v[4 * q + 2], mul * v[4 * q + 3]);
+            __syncwarp();
+        };
+        auto add_rows = [&](float* out, int c, int j) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int x = 4 * it + (lane >> 3), q = lane & 7;
+                const int jx = __shfl_sync(0xffffffffu, j, x);
+                const float4 w = *reinterpret_cast<const float4*>(xb + x * 32 + ((q ^ (x & 7)) * 4));
+                if (jx >= 0) red_add4(out + (seg_row0 + (int64_t)jx * a.Hkv) * D + c + 4 * q, w.x, w.y, w.z, w.w);
+            }
+            __syncwarp();
+        };
         bool ok = true;
         for (int k = 0; k < nblk && ok; ++k) {
             const int ridx = k % kIdxStages;
@@ -835,26 +860,21 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
             if (lane == 0) mbar_arrive(bar(kKBarIdxEmpty + ridx));
             if (!(ok = wait_warp(kKBarKVDone, k & 1))) break;
             tc_fence_after();
-            const int64_t row = (((int64_t)g.b * a.S + (j >= 0 ? j : 0)) * a.Hkv + g.h) * D;
-            float* dkr = a.dK + row;
-            float* dvr = a.dV + row;
+            // dK chunks (tensor-memory columns 256..), then dV chunks (384..); the MMA may overwrite
+            // both accumulators once the last chunk is in registers
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                float vk[32], vv[32];
-                tmem_ld32f(tm + 256 + lane_off + c, vk);
-                tmem_ld32f(tm + 384 + lane_off + c, vv);
+            for (int t = 0; t < 2 * (D / 32); ++t) {
+                const int c = (t % (D / 32)) * 32;
+                const bool is_v = t >= D / 32;
+                float v[32];
+                tmem_ld32f(tm + (is_v ? 384 : 256) + lane_off + c, v);
                 tmem_ld_wait();
-                if (c + 32 == D) {
+                if (t == 2 * (D / 32) - 1) {
                     tc_fence_before();
                     mbar_arrive(bar(kKBarKVFree));
                 }
-                if (j >= 0) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        red_add4(dkr + c + e, sc * vk[e], sc * vk[e + 1], sc * vk[e + 2], sc * vk[e + 3]);
-                        red_add4(dvr + c + e, vv[e], vv[e + 1], vv[e + 2], vv[e + 3]);
-                    }
-                }
+                put_row(v, is_v ? 1.f : sc);
+                add_rows(is_v ? a.dV : a.dK, c, j);
             }
         }
     } else {
