@@ -312,6 +312,81 @@ class Prefill:
         return a.elapsed_time(b) / steps, h2d_b, d2h_b
 
 
+# -------------------------------------------------------------- backward ----
+
+LAUNCHES_BACKWARD = 5  # delta/zero prep, row kernel, key kernel, score backward, its finalize (bf16)
+
+
+class Backward:
+    """The backward calls over a forward's kept sets (dQ, dK, dV, ds, then dW, dA and the score's
+    share of dV), with a seeded upstream gradient.  The forward's O, lse and selection must be in
+    place (Prefill.calls has run)."""
+
+    def __init__(self, dma, pf, seed=7):
+        self.dma, self.pf = dma, pf
+        cfg = pf.cfg
+        B, S, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        self.dO = torch.randn(pf.Q.shape, generator=g, device="cuda").to(pf.Q.dtype)
+        f32 = dict(dtype=torch.float32, device="cuda")
+        self.dQ = torch.empty((B, S, H, D), **f32)
+        self.dK = torch.empty((B, S, Hkv, D), **f32)
+        self.dV = torch.empty((B, S, Hkv, D), **f32)
+        self.ds = torch.empty((B, Hkv, S), **f32)
+        self.dW = torch.empty((Hkv, D), **f32)
+        self.dA = torch.empty((Hkv,), **f32) if pf.A is not None else None
+        self.ws = torch.empty((dma.dma_backward_workspace_size(B, S, H, Hkv, D),), dtype=torch.uint8, device="cuda")
+
+    def calls(self, stream, ev=None):
+        d, pf = self.dma, self.pf
+        if ev:
+            ev[0].record(stream)
+        d.dma_sparse_attn_prefill_backward(pf.Q, pf.K, pf.V, pf.scores, pf.kept, pf.O, pf.lse, self.dO, self.dQ,
+                                           self.dK, self.dV, self.ds, ws=self.ws, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        d.dma_score_keys_backward(pf.V, pf.W, pf.A, self.ds, self.dV, self.dW, self.dA, ws=self.ws, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    def timed(self, steps, warmup, world=1):
+        stream = torch.cuda.current_stream()
+        self.pf.calls(stream)
+        for _ in range(warmup):
+            self.calls(stream)
+        torch.cuda.synchronize()
+        assert self.dma.dma_get_device_status() == 0
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for s in range(steps):
+            self.calls(stream, ev[s])
+        torch.cuda.synchronize()
+        barrier(world)
+        assert self.dma.dma_get_device_status() == 0
+        a = max_over_ranks(statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(steps)), world)
+        b = max_over_ranks(statistics.mean(ev[s][1].elapsed_time(ev[s][2]) for s in range(steps)), world)
+        return {"attn_bwd_ms": a, "score_bwd_ms": b, "ms": a + b}
+
+
+def backward_entry(pf, r, peaks, steps):
+    """The backward's numbers for a workload: FLOPs by the usual convention of 2.5 times the
+    forward (S recomputed once, then dP, dQ, dK and dV: 10 D flop per kept pair)."""
+    cfg = pf.cfg
+    pairs = pf.pairs()
+    flops = 10.0 * cfg.D * pairs
+    tf = flops / (r["ms"] * 1e-3) / 1e12
+    ent = {"ms": round(r["ms"], 4), "attention_backward_ms": round(r["attn_bwd_ms"], 4),
+           "score_backward_ms": round(r["score_bwd_ms"], 4), "tflops": round(tf, 3),
+           "algorithmic": "10*D flop per kept (query, key) pair (5 products of 2*D; the kernels form "
+                          "S and dP in both the row and the key kernel: 14*D of tensor work)",
+           "gpu_launches": LAUNCHES_BACKWARD * steps}
+    if cfg.dtype != "f32":
+        ent["frac_of_bf16_peak"] = round(tf / peaks["bf16_tflops"], 4)
+        ent["tensor_work_frac_of_bf16_peak"] = round(tf * 1.4 / peaks["bf16_tflops"], 4)
+    return ent
+
+
 # ---------------------------------------------------------------- decode ----
 
 def bench_decode(args, world):
@@ -514,6 +589,7 @@ def main():
                     help="sequences of the decode workload (smaller values serve profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=4096, help="rows per (b, head) in the CPU-baseline sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per (b, head) per reference-arm step")
@@ -553,6 +629,13 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 3), "steps": ne,
                "overlap": "copies of one step overlap the compute of the step before (two buffer sets, "
                           "three streams)"}
+    bwd = None
+    if not args.no_backward:
+        bw = Backward(dma, pf)
+        bwd = backward_entry(pf, bw.timed(args.steps, args.warmup, world), peaks, args.steps)
+        bwd["workload"] = cfg.name
+        del bw
+        torch.cuda.empty_cache()
     per_config = {}
     if not args.no_per_config:
         for name in PER_CONFIG:
@@ -562,6 +645,11 @@ def main():
             else:
                 p = Prefill(dma, c)
             per_config[name] = per_config_entry(p, p.timed(args.steps, args.warmup, world), peaks)
+            if not args.no_backward and name != "prefill_s64k_block64_bf16":
+                bw = Backward(dma, p)
+                per_config[name]["backward"] = backward_entry(p, bw.timed(args.steps, args.warmup, world), peaks,
+                                                              args.steps)
+                del bw
             del p
             torch.cuda.empty_cache()
     dec = None if args.no_decode else bench_decode(args, world)
@@ -591,6 +679,8 @@ def main():
         "gpu_launches": launches + (0 if dec is None else LAUNCHES_PER_DECODE_STEP * args.steps),
         "clocks": clk,
     }
+    if bwd is not None:
+        line["backward"] = bwd
     if dec is not None:
         line["decode"] = {"workload": dec["workload"], "value": round(dec["gbs"], 2), "unit": "GB/s",
                           "frac_of_hbm": round(dec["gbs"] / peaks["hbm_gbs"], 4), "peak_gbs": peaks["hbm_gbs"],

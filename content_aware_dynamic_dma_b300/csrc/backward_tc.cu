@@ -171,9 +171,9 @@ __device__ __forceinline__ Geom tile_geom(const BwdArgs& a, int unit)
 // [lo, lo + tl)), then the flag "every row of the tile keeps every key of the block".
 constexpr int kIdxSlot = 5 * kBN * 4 + 16;
 
-// The metadata warp: fills slot t % kIdxStages for steps t = 0 .. nt-1, where step t walks key
+// The metadata warp: fills slot t % kStages for steps t = 0 .. nt-1, where step t walks key
 // block t % nblk.  `empty_base` / `full_base`: the ring's barrier slots.
-template <typename BarFn, typename WaitFn, typename SlotFn>
+template <int kStages, typename BarFn, typename WaitFn, typename SlotFn>
 __device__ __forceinline__ void meta_loop(const BwdArgs& a, const Geom& g, int nt, int lane, BarFn bar,
                                           WaitFn wait_warp, SlotFn idx_slot, int full_base, int empty_base)
 {
@@ -184,7 +184,7 @@ __device__ __forceinline__ void meta_loop(const BwdArgs& a, const Geom& g, int n
 #pragma unroll
     for (int e = 0; e < 4; ++e) jc[e] = g.key_at(4 * lane + e, a.S, a.status);
     for (int t = 0; t < nt; ++t) {
-        const int r = t % kIdxStages, use = t / kIdxStages;
+        const int r = t % kStages, use = t / kStages;
         if (use >= 1 && !wait_warp(empty_base + r, (use - 1) & 1)) break;
         float scv[4];
         int exv[4];
@@ -289,41 +289,55 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile) { return smem_de
 __device__ __forceinline__ uint32_t mnmajor_step(int kk) { return (uint32_t)(kk * (2048 >> 4)); }
 
 // =============================================================== row kernel (dQ)
-constexpr int kDqThreads = 384;  // EW warps 0-7, MMA 8, metadata 9, copies 10-11
-constexpr int kDqMma = 8, kDqMeta = 9, kDqCopy0 = 10;
-constexpr int kDqKStages = 3;
+// Q and dO of the pass's query head live in tensor memory as the A operand of S = Q K^T and
+// dP = dO V^T, so shared memory holds only gathered K and V rows, three blocks of each in
+// flight.  S and dP are single: S of the next block is computed as soon as the elementwise
+// warps have read this block's S into registers; dx is written over dP once dP has been read,
+// and is the A operand of dQ += dx K; the next dP follows that product.
+constexpr int kDqThreads = 640;  // EW warps 0-15, MMA 16, metadata 17, copies 18-19
+constexpr int kDqEwWarps = 16;   // 4 lane quarters x 4 column quarters
+constexpr int kDqMma = 16, kDqMeta = 17, kDqCopy0 = 18;
+constexpr int kDqStages = 3;     // K and V blocks in flight
+constexpr int kDqIdxStages = 6;
+// Registers per thread: 96 at launch (640 x 96 = 61,440); the control warps give registers to
+// the elementwise warps: 512 * 104 + 128 * 64 = 640 * 96.
+constexpr int kDqRegsEw = 104;
+constexpr int kDqRegsCtl = 64;
+static_assert(512 * kDqRegsEw + 128 * kDqRegsCtl <= kDqThreads * 96, "register split exceeds the launch's registers");
 
 enum : int {
-    kQBarQFull = 0,
-    kQBarQEmpty = 1,
-    kQBarKFull = 2,   // kDqKStages
-    kQBarKEmpty = 5,  // kDqKStages
-    kQBarVFull = 8,
-    kQBarVEmpty = 9,
-    kQBarSFull = 10,  // 2 (S buffer)
-    kQBarDPFull = 12,
-    kQBarDsReady = 13,
-    kQBarDQDone = 14,
-    kQBarDrain = 15,
-    kQBarPair = 16,  // 4 (lane quarters)
-    kQBarIdxFull = 20,
-    kQBarIdxEmpty = 20 + kIdxStages,
-    kQNumBars = 20 + 2 * kIdxStages
+    kQBarKFull = 0,   // kDqStages
+    kQBarKEmpty = 3,  // kDqStages
+    kQBarVFull = 6,   // kDqStages
+    kQBarVEmpty = 9,  // kDqStages
+    kQBarQReady = 12, // Q and dO of the pass in tensor memory (and the previous pass's dQ read out)
+    kQBarSFull = 13,
+    kQBarSRead = 14,
+    kQBarDPFull = 15,
+    kQBarDsReady = 16,
+    kQBarDQDone = 17,
+    kQBarDrain = 18,
+    kQBarQuad = 19,  // 4 (lane quarters)
+    kQBarIdxFull = 23,
+    kQBarIdxEmpty = 23 + kDqIdxStages,
+    kQNumBars = 23 + 2 * kDqIdxStages
 };
 
 template <int D>
 struct DqLayout {
     static constexpr int kTile = kBN * D * 2;
-    static constexpr int kQ = 0;
-    static constexpr int kdO = kTile;
-    static constexpr int kK = 2 * kTile;
-    static constexpr int kV = kK + kDqKStages * kTile;
-    static constexpr int kIdx = kV + kTile;
-    static constexpr int kBars = kIdx + kIdxStages * kIdxSlot;
+    static constexpr int kK = 0;
+    static constexpr int kV = kDqStages * kTile;
+    static constexpr int kIdx = 2 * kDqStages * kTile;
+    static constexpr int kBars = kIdx + kDqIdxStages * kIdxSlot;
     static constexpr int kMisc = kBars + 8 * kQNumBars;
     static constexpr int kEnd = kMisc + 16;
     static constexpr int kSmemBytes = kEnd + 1024;
 };
+static_assert(DqLayout<128>::kSmemBytes <= 227 * 1024, "row kernel shared memory");
+
+// tensor-memory columns of the row kernel
+constexpr uint32_t kTmDQ = 0, kTmQ = 128, kTmDO = 192, kTmS = 256, kTmDP = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs a, const uint64_t wait_ns)
@@ -357,14 +371,17 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < kQNumBars; ++i) mbar_init(bar(i), 1);
-        mbar_init(bar(kQBarQFull), kCopyThreads);
-        for (int s = 0; s < kDqKStages; ++s) mbar_init(bar(kQBarKFull + s), kCopyThreads);
-        mbar_init(bar(kQBarVFull), kCopyThreads);
-        mbar_init(bar(kQBarDsReady), 32 * kEwWarps);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(kQBarPair + q), 2);
-        for (int r = 0; r < kIdxStages; ++r) {
+        for (int s = 0; s < kDqStages; ++s) {
+            mbar_init(bar(kQBarKFull + s), kCopyThreads);
+            mbar_init(bar(kQBarVFull + s), kCopyThreads);
+        }
+        mbar_init(bar(kQBarQReady), 32 * kDqEwWarps);
+        mbar_init(bar(kQBarSRead), 32 * kDqEwWarps);
+        mbar_init(bar(kQBarDsReady), 32 * kDqEwWarps);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(kQBarQuad + q), 4);
+        for (int r = 0; r < kDqIdxStages; ++r) {
             mbar_init(bar(kQBarIdxFull + r), 32);
-            mbar_init(bar(kQBarIdxEmpty + r), kEwWarps + 2);  // EW warps and the two copy warps
+            mbar_init(bar(kQBarIdxEmpty + r), kDqEwWarps + 2);  // EW warps and the two copy warps
         }
         mbar_init_fence();
     }
@@ -374,141 +391,162 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
     tc_fence_after();
 
     if (warp == kDqMeta) {
+        regs_decrease<kDqRegsCtl>();
         const Geom g = tile_geom(a, fresh_ctaid());
-        meta_loop(a, g, G * g.nblk, lane, bar, wait_warp, idx_slot, kQBarIdxFull, kQBarIdxEmpty);
+        meta_loop<kDqIdxStages>(a, g, G * g.nblk, lane, bar, wait_warp, idx_slot, kQBarIdxFull, kQBarIdxEmpty);
     } else if (warp >= kDqCopy0) {
+        regs_decrease<kDqRegsCtl>();
         const Geom g = tile_geom(a, fresh_ctaid());
-        const int nblk = g.nblk, n = G * nblk;
+        const int n = G * g.nblk;
         const RowCopier<D> cp(threadIdx.x - kDqCopy0 * 32);
         const int64_t kv_stride = (int64_t)a.Hkv * D;
         const __nv_bfloat16* Kh = static_cast<const __nv_bfloat16*>(a.K) + ((int64_t)g.b * a.S * a.Hkv + g.h) * D;
         const __nv_bfloat16* Vh = static_cast<const __nv_bfloat16*>(a.V) + ((int64_t)g.b * a.S * a.Hkv + g.h) * D;
-        const int64_t q_stride = (int64_t)a.H * D;
         bool ok = true;
         for (int u = 0; u < n && ok; ++u) {
-            const int gq = u / nblk, k = u % nblk;
-            if (k == 0) {
-                if (gq > 0 && !(ok = wait_warp(kQBarQEmpty, (gq - 1) & 1))) break;
-                const int64_t off = ((int64_t)g.b * a.S * a.H + g.h * G + gq) * D;
-                cp.rows(sbase + L::kQ, g.q0, a.S, static_cast<const __nv_bfloat16*>(a.Q) + off, q_stride);
-                cp.rows(sbase + L::kdO, g.q0, a.S, static_cast<const __nv_bfloat16*>(a.dO) + off, q_stride);
-                cp_async_arrive(bar(kQBarQFull));
-            }
-            const int r = u % kIdxStages, ks = u % kDqKStages;
-            if (!(ok = wait_warp(kQBarIdxFull + r, (u / kIdxStages) & 1))) break;
-            if (u >= kDqKStages && !(ok = wait_warp(kQBarKEmpty + ks, (u / kDqKStages - 1) & 1))) break;
-            cp.gather(sbase + L::kK + ks * L::kTile, idx_slot(r), Kh, kv_stride);
-            cp_async_arrive(bar(kQBarKFull + ks));
-            if (u >= 1 && !(ok = wait_warp(kQBarVEmpty, (u - 1) & 1))) break;
-            cp.gather(sbase + L::kV, idx_slot(r), Vh, kv_stride);
-            cp_async_arrive(bar(kQBarVFull));
+            const int r = u % kDqIdxStages, st = u % kDqStages, use = u / kDqStages;
+            if (!(ok = wait_warp(kQBarIdxFull + r, (u / kDqIdxStages) & 1))) break;
+            if (use >= 1 && !(ok = wait_warp(kQBarKEmpty + st, (use - 1) & 1))) break;
+            cp.gather(sbase + L::kK + st * L::kTile, idx_slot(r), Kh, kv_stride);
+            cp_async_arrive(bar(kQBarKFull + st));
+            if (use >= 1 && !(ok = wait_warp(kQBarVEmpty + st, (use - 1) & 1))) break;
+            cp.gather(sbase + L::kV + st * L::kTile, idx_slot(r), Vh, kv_stride);
+            cp_async_arrive(bar(kQBarVFull + st));
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kQBarIdxEmpty + r));
         }
         cp_async_wait_all();
     } else if (warp == kDqMma) {
+        regs_decrease<kDqRegsCtl>();
         const Geom g = tile_geom(a, fresh_ctaid());
-        const int nblk = g.nblk, n = G * nblk;
+        const int nblk = g.nblk;
         const uint32_t tm = *tmem_slot;
-        const uint32_t tDQ = tm, tDP = tm + 384;
         const bool leader = lane == 0;
         constexpr uint32_t idS = idesc_bf16_f32(128, kBN, false);
         constexpr uint32_t idQ = idesc_bf16_f32(128, D, true);
         auto commit = [&](int barid) {
             if (leader) mma_commit(bar(barid));
         };
-        auto issue_s = [&](int u) {
-            const uint64_t dq = kmajor_desc(sbase + L::kQ);
-            const uint64_t dk = kmajor_desc(sbase + L::kK + (u % kDqKStages) * L::kTile);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                if (leader) mma_ss(tm + 128 + 128 * (u & 1), dq + kmajor_step(kk), dk + kmajor_step(kk), idS, kk > 0);
-        };
-        auto issue_dp = [&]() {
-            const uint64_t dg = kmajor_desc(sbase + L::kdO);
-            const uint64_t dv = kmajor_desc(sbase + L::kV);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                if (leader) mma_ss(tDP, dg + kmajor_step(kk), dv + kmajor_step(kk), idS, kk > 0);
-        };
-        auto issue_dq = [&](int u, bool first) {
-            const uint64_t dk = mnmajor_desc(sbase + L::kK + (u % kDqKStages) * L::kTile);
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-                if (leader)
-                    mma_ts(tDQ, tm + 128 + 128 * (u & 1) + kk * 8, dk + mnmajor_step(kk), idQ, (first && kk == 0) ? 0u : 1u);
-        };
-        // S(u): Q of the pass (waited for at the pass's first block) and K(u)
+        // S(u) = Q K(u)^T and dP(u) = dO V(u)^T: A from tensor memory, B K-major in shared memory
         auto start_s = [&](int u) -> bool {
-            if (u % nblk == 0 && !wait_warp(kQBarQFull, (u / nblk) & 1)) return false;
-            if (!wait_warp(kQBarKFull + u % kDqKStages, (u / kDqKStages) & 1)) return false;
+            const int st = u % kDqStages;
+            if (!wait_warp(kQBarKFull + st, (u / kDqStages) & 1)) return false;
             fence_proxy_async_smem();
             tc_fence_after();
-            issue_s(u);
-            commit(kQBarSFull + (u & 1));
+            const uint64_t dk = kmajor_desc(sbase + L::kK + st * L::kTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader) mma_ts(tm + kTmS, tm + kTmQ + kk * 8, dk + kmajor_step(kk), idS, kk > 0);
+            commit(kQBarSFull);
             return true;
         };
         auto start_dp = [&](int u) -> bool {
-            if (!wait_warp(kQBarVFull, u & 1)) return false;
+            const int st = u % kDqStages;
+            if (!wait_warp(kQBarVFull + st, (u / kDqStages) & 1)) return false;
             fence_proxy_async_smem();
             tc_fence_after();
-            issue_dp();
+            const uint64_t dv = kmajor_desc(sbase + L::kV + st * L::kTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader) mma_ts(tm + kTmDP, tm + kTmDO + kk * 8, dv + kmajor_step(kk), idS, kk > 0);
             commit(kQBarDPFull);
-            commit(kQBarVEmpty);
-            if (u % nblk == nblk - 1) commit(kQBarQEmpty);  // the pass's last S and dP are issued
+            commit(kQBarVEmpty + st);
             return true;
         };
-        bool ok = start_s(0) && start_dp(0) && (n < 2 || start_s(1));
-        for (int u = 0; u < n && ok; ++u) {
-            if (!(ok = wait_warp(kQBarDsReady, u & 1))) break;
+        bool ok = true;
+        for (int gq = 0; gq < G && ok; ++gq) {
+            const int u0 = gq * nblk;
+            // this pass's Q and dO are in tensor memory (the previous pass's dQ has been read out)
+            if (!(ok = wait_warp(kQBarQReady, gq & 1))) break;
             tc_fence_after();
-            issue_dq(u, u % nblk == 0);
-            commit(kQBarKEmpty + u % kDqKStages);
-            if (u % nblk == nblk - 1) commit(kQBarDQDone);
-            if (u + 1 < n && !(ok = start_dp(u + 1))) break;
-            if (u + 2 < n && !(ok = start_s(u + 2))) break;
+            if (!(ok = start_s(u0) && start_dp(u0))) break;
+            for (int k = 0; k < nblk; ++k) {
+                const int u = u0 + k;
+                if (k + 1 < nblk) {
+                    // the next S as soon as this one has been read
+                    if (!(ok = wait_warp(kQBarSRead, u & 1))) break;
+                    if (!(ok = start_s(u + 1))) break;
+                }
+                if (!(ok = wait_warp(kQBarDsReady, u & 1))) break;
+                tc_fence_after();
+                const uint64_t dk = mnmajor_desc(sbase + L::kK + (u % kDqStages) * L::kTile);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    if (leader)
+                        mma_ts(tm + kTmDQ, tm + kTmDP + kk * 8, dk + mnmajor_step(kk), idQ, (k == 0 && kk == 0) ? 0u : 1u);
+                commit(kQBarKEmpty + u % kDqStages);
+                if (k + 1 < nblk && !(ok = start_dp(u + 1))) break;
+            }
+            if (!ok) break;
+            commit(kQBarDQDone);
         }
         commit(kQBarDrain);
         if (leader) mbar_wait_drain(bar(kQBarDrain), 0, wait_ns);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ elementwise
-        // Thread = query row r (tensor-memory lane), key columns [64 hh, 64 hh + 64) of a block.
+        // Thread = query row r (tensor-memory lane) and key columns [32 cq, 32 cq + 32) of a block.
+        regs_increase<kDqRegsEw>();
         const Geom g = tile_geom(a, fresh_ctaid());
         const int nblk = g.nblk, q0 = g.q0, W = g.W;
         const uint32_t tm = *tmem_slot;
-        const int quarter = warp & 3, hh = warp >> 2;
+        const int quarter = warp & 3, cq = warp >> 2;
         const int r = quarter * 32 + lane, i = q0 + r;
         const bool valid = i < a.S;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const f2 cc2 = mk2(a.scale * kLog2e, a.scale * kLog2e);
+        constexpr int kQC = D / 8;  // packed Q (and dO) columns of this thread: D / 4 elements
         bool ok = true;
         for (int gq = 0; gq < G && ok; ++gq) {
             const int hq = g.h * G + gq;
+            // Q and dO of the pass into tensor memory (bf16 pairs, the A operand layout)
+            {
+                const int64_t qo = (((int64_t)g.b * a.S + min(i, a.S - 1)) * a.H + hq) * D + cq * (D / 4);
+                const uint4* qs = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.Q) + qo);
+                const uint4* gs = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dO) + qo);
+                uint32_t qv[kQC], gv[kQC];
+#pragma unroll
+                for (int c = 0; c < kQC / 4; ++c) {
+                    const uint4 x = valid ? __ldg(qs + c) : make_uint4(0, 0, 0, 0);
+                    const uint4 y = valid ? __ldg(gs + c) : make_uint4(0, 0, 0, 0);
+                    qv[4 * c] = x.x; qv[4 * c + 1] = x.y; qv[4 * c + 2] = x.z; qv[4 * c + 3] = x.w;
+                    gv[4 * c] = y.x; gv[4 * c + 1] = y.y; gv[4 * c + 2] = y.z; gv[4 * c + 3] = y.w;
+                }
+                if constexpr (kQC == 16) {
+                    tmem_st16(tm + kTmQ + lane_off + cq * kQC, qv);
+                    tmem_st16(tm + kTmDO + lane_off + cq * kQC, gv);
+                } else {
+                    tmem_st8(tm + kTmQ + lane_off + cq * kQC, qv);
+                    tmem_st8(tm + kTmDO + lane_off + cq * kQC, gv);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kQBarQReady));
+            }
             const int64_t rs = ((int64_t)g.b * a.H + hq) * a.S + i;
             float lse_l2 = valid ? a.lse[rs] * kLog2e : INFINITY;
             if (lse_l2 == -INFINITY) lse_l2 = INFINITY;  // a row that keeps nothing contributes nothing
             const float dl = valid ? a.delta[rs] : 0.f;
             const f2 nl2 = mk2(-lse_l2, -lse_l2), dl2 = mk2(dl, dl);
-            f2 dsum2 = mk2(0.f, 0.f);  // sum of p dP over this half's keys: the summed form of Delta
+            f2 dsum2 = mk2(0.f, 0.f);  // sum of p dP over this thread's keys: the summed form of Delta
             for (int k = 0; k < nblk; ++k) {
-                const int u = gq * nblk + k, ridx = u % kIdxStages;
-                ok = wait_warp(kQBarIdxFull + ridx, (u / kIdxStages) & 1) && wait_warp(kQBarSFull + (u & 1), (u >> 1) & 1);
+                const int u = gq * nblk + k, ridx = u % kDqIdxStages;
+                ok = wait_warp(kQBarIdxFull + ridx, (u / kDqIdxStages) & 1) && wait_warp(kQBarSFull, u & 1);
                 if (!ok) break;
                 tc_fence_after();
                 const int* js = idx_slot(ridx);
-                const float* mb = reinterpret_cast<const float*>(js + kBN) + 64 * hh;
-                const int* mj = js + 2 * kBN + 64 * hh;
-                const int* mlo = js + 3 * kBN + 64 * hh;
-                const int* mtl = js + 4 * kBN + 64 * hh;
+                const float* mb = reinterpret_cast<const float*>(js + kBN) + 32 * cq;
+                const int* mj = js + 2 * kBN + 32 * cq;
+                const int* mlo = js + 3 * kBN + 32 * cq;
+                const int* mtl = js + 4 * kBN + 32 * cq;
                 const bool all_full = js[5 * kBN] != 0;
-                const uint32_t tS = tm + 128 + 128 * (u & 1) + lane_off;
-                float p[64];
-                tmem_ld32f(tS + 64 * hh, p);
-                tmem_ld32f(tS + 64 * hh + 32, p + 32);
+                float p[32];
+                tmem_ld32f(tm + kTmS + lane_off + 32 * cq, p);
                 tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(bar(kQBarSRead));
 #pragma unroll
-                for (int c = 0; c < 64; c += 4) {
+                for (int c = 0; c < 32; c += 4) {
                     const float4 bb = *reinterpret_cast<const float4*>(mb + c);
                     f2 x01 = add2(fma2(mk2(p[c], p[c + 1]), cc2, mk2(bb.x, bb.y)), nl2);
                     f2 x23 = add2(fma2(mk2(p[c + 2], p[c + 3]), cc2, mk2(bb.z, bb.w)), nl2);
@@ -532,26 +570,25 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
                 }
                 if (!(ok = wait_warp(kQBarDPFull, u & 1))) break;
                 tc_fence_after();
-                float dp[64];
-                tmem_ld32f(tm + 384 + lane_off + 64 * hh, dp);
-                tmem_ld32f(tm + 384 + lane_off + 64 * hh + 32, dp + 32);
+                float dp[32];
+                tmem_ld32f(tm + kTmDP + lane_off + 32 * cq, dp);
                 tmem_ld_wait();
-                // both column halves of this lane quarter have read S and dP before either writes
+                // the four column quarters of this lane quarter have read dP before any writes dx
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kQBarPair + quarter));
-                if (!(ok = wait_warp(kQBarPair + quarter, u & 1))) break;
+                if (lane == 0) mbar_arrive(bar(kQBarQuad + quarter));
+                if (!(ok = wait_warp(kQBarQuad + quarter, u & 1))) break;
                 tc_fence_after();
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
+                for (int e = 0; e < 32; e += 2) {
                     const f2 p2 = mk2(p[e], p[e + 1]), dp2 = mk2(dp[e], dp[e + 1]);
                     dsum2 = fma2(p2, dp2, dsum2);
                     float d0, d1;
                     split2(mul2(p2, sub2(dp2, dl2)), d0, d1);
                     pk[e / 2] = pack_bf16(d0, d1);
                 }
-                tmem_st32(tS + 32 * hh, pk);
+                tmem_st16(tm + kTmDP + lane_off + 16 * cq, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(kQBarDsReady));
@@ -562,22 +599,32 @@ __global__ void __launch_bounds__(kDqThreads, 1) bwd_dq_tc_kernel(const BwdArgs 
             if (valid) {
                 float d0, d1;
                 split2(dsum2, d0, d1);
-                atomicAdd(a.delta_x + rs, d0 + d1);  // the two column halves of the row
+                atomicAdd(a.delta_x + rs, d0 + d1);  // the four column quarters of the row
             }
             // the pass's dQ: scale * accumulator, fp32
             if (!(ok = wait_warp(kQBarDQDone, gq & 1))) break;
             tc_fence_after();
-            float* dq = a.dQ + (((int64_t)g.b * a.S + min(i, a.S - 1)) * a.H + hq) * D + hh * (D / 2);
-#pragma unroll
-            for (int c = 0; c < D / 2; c += 32) {
+            float* dq = a.dQ + (((int64_t)g.b * a.S + min(i, a.S - 1)) * a.H + hq) * D + cq * (D / 4);
+            if constexpr (D == 128) {
                 float v[32];
-                tmem_ld32f(tm + lane_off + hh * (D / 2) + c, v);
+                tmem_ld32f(tm + kTmDQ + lane_off + cq * 32, v);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(dq + c + e) =
+                        *reinterpret_cast<float4*>(dq + e) =
                             make_float4(a.scale * v[e], a.scale * v[e + 1], a.scale * v[e + 2], a.scale * v[e + 3]);
+                }
+            } else {
+                uint32_t v[16];
+                tmem_ld16(tm + kTmDQ + lane_off + cq * 16, v);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4*>(dq + e) =
+                            make_float4(a.scale * __uint_as_float(v[e]), a.scale * __uint_as_float(v[e + 1]),
+                                        a.scale * __uint_as_float(v[e + 2]), a.scale * __uint_as_float(v[e + 3]));
                 }
             }
             tc_fence_before();
@@ -687,7 +734,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1) bwd_dkv_tc_kernel(const BwdArg
     if (warp == kKvMeta) {
         regs_decrease<kRegsOther>();
         const Geom g = tile_geom(a, fresh_ctaid());
-        meta_loop(a, g, g.nblk, lane, bar, wait_warp, idx_slot, kKBarIdxFull, kKBarIdxEmpty);
+        meta_loop<kIdxStages>(a, g, g.nblk, lane, bar, wait_warp, idx_slot, kKBarIdxFull, kKBarIdxEmpty);
     } else if (warp >= kKvCopy0) {
         regs_decrease<kRegsOther>();
         const Geom g = tile_geom(a, fresh_ctaid());
