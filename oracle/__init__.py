@@ -208,6 +208,43 @@ def backward(Q, K, V, W, A, w: int, window: int, dO, block: int = 1, mode: int =
     return dQ, dK, dV + dV2, dW, dA
 
 
+def page_scores(scores, cache_len, page_size: int) -> torch.Tensor:
+    """Page score of a paged cache (Sparse Frontier summary, decode findings: page-level
+    selection; the page's score is the maximum of its keys' scores, as for 64-key blocks):
+    ps[b][h][p] = max of scores[b][h][j] over the keys j < cache_len[b] of logical page p
+    (keys p*page_size .. p*page_size + page_size - 1); -inf for a page with none.  fp64."""
+    B, Hkv, Lmax = scores.shape
+    n_pages = (Lmax + page_size - 1) // page_size
+    out = torch.full((B, Hkv, n_pages), -math.inf, dtype=torch.float64)
+    s = scores.to(torch.float64)
+    for b in range(B):
+        L = int(cache_len[b])
+        for p in range((L + page_size - 1) // page_size):
+            out[b, :, p] = s[b, :, p * page_size:min(L, (p + 1) * page_size)].max(dim=-1).values
+    return out
+
+
+def select_pages(scores, cache_len, page_size: int, w: int):
+    """Kept pages of the decode row L-1 (L = cache_len[b]) for every (b, KV head): among the
+    complete pages (last key <= L-1), the floor(w / page_size) with the highest page score,
+    ties to the lower page index; scores compared as fp32 (-0 equals +0), as the selection
+    does.  Returns {(b, h): sorted list of kept page indices}."""
+    B, Hkv, _ = scores.shape
+    k = w // page_size
+    out = {}
+    for b in range(B):
+        L = int(cache_len[b])
+        n_c = L // page_size
+        for h in range(Hkv):
+            vals = []
+            for p in range(n_c):
+                v = max(float(np.float32(x)) + 0.0 for x in scores[b, h, p * page_size:(p + 1) * page_size].tolist())
+                vals.append((-v, p))
+            vals.sort()
+            out[(b, h)] = sorted(p for _, p in vals[:k])
+    return out
+
+
 def top_lo(j, block: int):
     """First row at which key j may enter the top set (its block's last key)."""
     if block <= 1:

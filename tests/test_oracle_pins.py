@@ -457,3 +457,30 @@ def test_golden_equal_scores_uniform_weights(oracle_mod, mode):
         want, n = O[i]
         assert torch.allclose(out[0, i, 0], torch.tensor(want, dtype=torch.float64), atol=1e-12, rtol=0), i
         assert abs(float(lse[0, 0, i]) - (math.log(2.0) + math.log(n))) < 1e-12, i
+
+
+# ------------------------------------------------------------- paged pages --
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_select_pages_is_block_selection_of_the_last_row(oracle_mod, page_size):
+    """Page selection of the decode row L-1 equals the block-unit selection (block = page size)
+    of that row, computed by the pinned selection oracle on the first L keys; the page score is
+    the maximum of the page's key scores (checked against numpy's max)."""
+    B, Hkv, Lmax, w = 3, 2, 700, 200
+    g = torch.Generator().manual_seed(17)
+    scores = torch.randn((B, Hkv, Lmax), generator=g, dtype=torch.float64)
+    scores[0, 0, 100:300] = 0.5  # ties across pages
+    lens = [700, 513, page_size * 3 - 1]
+    ps = oracle_mod.page_scores(scores, lens, page_size)
+    kept = oracle_mod.select_pages(scores, lens, page_size, w)
+    for b in range(B):
+        L = lens[b]
+        ex = oracle_mod.select(scores[b:b + 1, :, :L], w, block=page_size)
+        for h in range(Hkv):
+            for p in range((L + page_size - 1) // page_size):
+                want = np.max(scores[b, h, p * page_size:min(L, (p + 1) * page_size)].numpy())
+                assert float(ps[b, h, p]) == float(want)
+            top = oracle_mod.top_set(ex[0, h], L - 1, block=page_size)
+            keys = sorted(j for p in kept[(b, h)] for j in range(p * page_size, (p + 1) * page_size))
+            assert keys == sorted(top), (b, h)
+            assert len(kept[(b, h)]) == min(w // page_size, L // page_size)
