@@ -13,10 +13,12 @@ The functions carry the C names:
 * ``dma_sparse_attn_decode``  the same for one new query row per sequence
 * ``dma_sparse_attn_prefill_backward``  dQ, dK, dV and ds over the kept pairs
 * ``dma_score_keys_backward``  ds -> dW, dA and the score's share of dV
+* ``dma_score_keys_paged``, ``dma_select_pages``, ``dma_sparse_attn_decode_paged``
+  page-granular decode over a paged KV cache
 
-plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and three
-compositions, ``prefill``, ``prefill_backward`` and ``DecodeState``, for the
-common call sequences.
+plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and four
+compositions, ``prefill``, ``prefill_backward``, ``DecodeState`` and
+``PagedDecodeState``, for the common call sequences.
 """
 from __future__ import annotations
 
@@ -65,7 +67,8 @@ EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_
             "dma_decode_workspace_size", "dma_sparse_attn_decode", "dma_sparse_attn_decode_noalloc",
             "dma_get_device_status", "dma_status_string", "dma_last_error_message", "dma_set_prefill_kernel",
             "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version", "dma_backward_workspace_size",
-            "dma_sparse_attn_prefill_backward", "dma_score_keys_backward")
+            "dma_sparse_attn_prefill_backward", "dma_score_keys_backward", "dma_score_keys_paged",
+            "dma_select_pages", "dma_sparse_attn_decode_paged")
 
 
 def _load_lib():
@@ -93,6 +96,9 @@ def _load_lib():
         "dma_backward_workspace_size": [I, I, I, I, I, ctypes.POINTER(Z)],
         "dma_sparse_attn_prefill_backward": [P, P, P, I, I, I, I, I, I, P, PK, F, P, P, P, P, P, P, P, P, Z, P],
         "dma_score_keys_backward": [P, I, I, I, I, I, P, P, P, P, P, P, P, Z, P],
+        "dma_score_keys_paged": [P, I, I, P, I, I, I, P, I, I, I, I, P, P, P, P, P],
+        "dma_select_pages": [P, I, I, I, I, P, I, P, P, I, P],
+        "dma_sparse_attn_decode_paged": [P, P, P, I, I, P, I, I, I, P, I, I, I, P, P, P, I, I, F, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -296,6 +302,41 @@ def dma_score_keys_backward(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.
                                         _stream(stream)))
 
 
+def dma_score_keys_paged(V_pages: torch.Tensor, block_table: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor],
+                         scores: torch.Tensor, page_scores: Optional[torch.Tensor] = None,
+                         cache_len: Optional[torch.Tensor] = None, key_begin: int = 0, key_end: Optional[int] = None,
+                         stream=None) -> None:
+    """V_pages [n_pages][page_size][Hkv][D]; block_table [B][max_pages] int32; scores
+    [B][Hkv][max_pages * page_size]; page_scores [B][Hkv][max_pages] (fp32)."""
+    n_pages, P, Hkv, D = V_pages.shape
+    B, max_pages = block_table.shape
+    key_end = max_pages * P if key_end is None else key_end
+    _check(_lib.dma_score_keys_paged(_ptr(V_pages), _dtype(V_pages), n_pages, _ptr(block_table), B, max_pages, P,
+                                     _ptr(cache_len), Hkv, D, key_begin, key_end, _ptr(W), _ptr(A), _ptr(scores),
+                                     _ptr(page_scores), _stream(stream)))
+
+
+def dma_select_pages(page_scores: torch.Tensor, page_size: int, w: int, top_idx: torch.Tensor,
+                     top_count: torch.Tensor, cache_len: Optional[torch.Tensor] = None, stream=None) -> None:
+    B, Hkv, max_pages = page_scores.shape
+    _check(_lib.dma_select_pages(_ptr(page_scores), B, Hkv, max_pages, page_size, _ptr(cache_len), w, _ptr(top_idx),
+                                 _ptr(top_count), top_idx.shape[-1], _stream(stream)))
+
+
+def dma_sparse_attn_decode_paged(q: torch.Tensor, K_pages: torch.Tensor, V_pages: torch.Tensor,
+                                 block_table: torch.Tensor, scores: torch.Tensor, top_idx: torch.Tensor,
+                                 top_count: torch.Tensor, window: int, o: torch.Tensor, ws: torch.Tensor,
+                                 lse: Optional[torch.Tensor] = None, cache_len: Optional[torch.Tensor] = None,
+                                 scale: float = 0.0, stream=None) -> None:
+    B, H, D = q.shape
+    n_pages, P, Hkv, _ = K_pages.shape
+    max_pages = block_table.shape[1]
+    _check(_lib.dma_sparse_attn_decode_paged(
+        _ptr(q), _ptr(K_pages), _ptr(V_pages), _dtype(q), n_pages, _ptr(block_table), B, max_pages, P,
+        _ptr(cache_len), H, Hkv, D, _ptr(scores), _ptr(top_idx), _ptr(top_count), top_idx.shape[-1], window,
+        float(scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
 def dma_get_device_status(stream=None) -> int:
     v = ctypes.c_int(0)
     _check(_lib.dma_get_device_status(_stream(stream), ctypes.byref(v)))
@@ -399,3 +440,38 @@ class DecodeState:
         dma_score_keys(Vc, W, A, self.scores, new_pos, new_pos + 1, stream=stream)
         dma_select_topk(self.scores, self.kept, UPDATE, seq_len=cache_len, stream=stream)
         dma_sparse_attn_decode(q, Kc, Vc, self.scores, self.kept, o, self.ws, lse, cache_len, scale, stream=stream)
+
+
+class PagedDecodeState:
+    """Decode-side buffers for a paged KV cache: the key and page score caches, the kept keys of
+    the selected pages and the workspace."""
+
+    def __init__(self, B: int, max_pages: int, page_size: int, H: int, Hkv: int, D: int, w: int, window: int,
+                 device="cuda"):
+        self.B, self.max_pages, self.page_size, self.H, self.Hkv, self.D = B, max_pages, page_size, H, Hkv, D
+        self.w, self.window = w, window
+        f32 = dict(dtype=torch.float32, device=device)
+        self.scores = torch.zeros((B, Hkv, max_pages * page_size), **f32)
+        self.page_scores = torch.full((B, Hkv, max_pages), float("-inf"), **f32)
+        self.top_cap = max(1, (w // page_size) * page_size)
+        self.top_idx = torch.zeros((B, Hkv, self.top_cap), dtype=torch.int32, device=device)
+        self.top_count = torch.zeros((B, Hkv), dtype=torch.int32, device=device)
+        self.ws = torch.empty((dma_decode_workspace_size(B, H, Hkv, D, self.top_cap, window),), dtype=torch.uint8,
+                              device=device)
+
+    def full_score(self, V_pages, block_table, W, A=None, cache_len=None, length: Optional[int] = None, stream=None):
+        """Scores every key below ``length`` (all of the cache when None) and its page scores."""
+        length = self.max_pages * self.page_size if length is None else length
+        dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, 0, length,
+                             stream=stream)
+
+    def step(self, q, K_pages, V_pages, block_table, W, cache_len: torch.Tensor, new_pos: int, o, lse=None, A=None,
+             scale: float = 0.0, stream=None):
+        """One decode step for a token already written at logical position ``new_pos``
+        (= cache_len - 1): score it, update its page's score, select the pages, attend."""
+        dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, new_pos,
+                             new_pos + 1, stream=stream)
+        dma_select_pages(self.page_scores, self.page_size, self.w, self.top_idx, self.top_count, cache_len,
+                         stream=stream)
+        dma_sparse_attn_decode_paged(q, K_pages, V_pages, block_table, self.scores, self.top_idx, self.top_count,
+                                     self.window, o, self.ws, lse, cache_len, scale, stream=stream)

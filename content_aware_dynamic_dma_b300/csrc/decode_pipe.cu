@@ -45,8 +45,9 @@ struct PipeLayout {
     static constexpr int kMerge = 0;  // [warp][16][D + 2] f32, over the stages once the pipeline is drained
     static_assert(kConsumerWarps * 16 * (D + 2) * 4 <= kBias, "merge area must fit in the stages");
     static constexpr int kKeys = kBias + kStages * kStageKeys * 4;  // the split's key list (runtime length)
-    // bytes of shared memory for a split of at most `max_keys` keys (1024 of slack for alignment)
-    static constexpr int smem_bytes(int max_keys) { return kKeys + max_keys * 4 + 1024; }
+    // bytes of shared memory for a split of at most `max_keys` keys, then (paged cache) the
+    // sequence's `bt_entries` block-table entries (1024 of slack for alignment)
+    static constexpr int smem_bytes(int max_keys, int bt_entries = 0) { return kKeys + (max_keys + bt_entries) * 4 + 1024; }
 };
 
 struct PipeArgs {
@@ -59,6 +60,10 @@ struct PipeArgs {
     float* part_ml;             // [B * H][nsplit][2]  (max in log2 units, sum)
     int B, Lmax, H, Hkv, G, top_cap, window, nsplit;
     float c_log2;               // scale * log2(e)
+    // paged cache: K/V pages [n_pages][1 << pshift][Hkv][D], block_table [B][max_pages]
+    const int32_t* block_table;
+    int n_pages, max_pages, pshift;
+    int* status;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
@@ -117,7 +122,9 @@ __device__ __forceinline__ int list_key(int u, const int32_t* top, int n_top, in
     return (j >= 0 && j <= L - 1) ? j : -1;
 }
 
-template <int D>
+// kPaged: Kc and Vc are K/V pages; key j of sequence b is row
+// (block_table[b][j >> pshift] << pshift) + (j & (page size - 1)) of them.
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv_bfloat16* __restrict__ Kc,
                                                                       const __nv_bfloat16* __restrict__ Vc,
                                                                       const PipeArgs a)
@@ -155,8 +162,8 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     const int32_t* top = a.top_idx + (int64_t)seg * a.top_cap;
     const float* sc = a.scores + (int64_t)seg * a.Lmax;
     const int64_t row_stride = (int64_t)a.Hkv * D;
-    const __nv_bfloat16* Kh = Kc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
-    const __nv_bfloat16* Vh = Vc + ((int64_t)b * a.Lmax * a.Hkv + h) * D;
+    const __nv_bfloat16* Kh = Kc + (kPaged ? (int64_t)h * D : ((int64_t)b * a.Lmax * a.Hkv + h) * D);
+    const __nv_bfloat16* Vh = Vc + (kPaged ? (int64_t)h * D : ((int64_t)b * a.Lmax * a.Hkv + h) * D);
 
     // Key indices: the whole split's key list is read into shared memory once, before the first
     // copies (a per-stage index load would put its latency into every stage); the copies (chunk
@@ -165,6 +172,30 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
     const int n_keys = u_end - u_begin;
     for (int i = threadIdx.x; i < n_keys; i += kPipeThreads)
         keys_s[i] = list_key(u_begin + i, top, n_top, L, a.window);
+    // paged cache: the sequence's block-table entries for pages 0 .. (L - 1) >> pshift (an entry
+    // outside [0, n_pages) marks its page's rows as unreadable: recorded, and read as zeros)
+    int* bt_s = keys_s + n_keys;
+    if constexpr (kPaged) {
+        const int n_pg = ((L - 1) >> a.pshift) + 1;
+        for (int i = threadIdx.x; i < n_pg; i += kPipeThreads) {
+            int phys = a.block_table[(int64_t)b * a.max_pages + i];
+            if (phys < 0 || phys >= a.n_pages) {
+                set_status(a.status, DMA_ERR_DEVICE_CHECK);
+                phys = -1;
+            }
+            bt_s[i] = phys;
+        }
+    }
+    // the row of key j in Kh / Vh, or -1
+    auto key_row = [&](int j) -> int64_t {
+        if constexpr (kPaged) {
+            if (j < 0) return -1;
+            const int phys = bt_s[j >> a.pshift];
+            return phys < 0 ? -1 : ((int64_t)phys << a.pshift) + (j & ((1 << a.pshift) - 1));
+        } else {
+            return j;
+        }
+    };
     const int part = threadIdx.x % kCPR, r0 = threadIdx.x / kCPR;
     auto key_at = [&](int st, int r) -> int {
         const int i = st * kStageKeys + r;
@@ -177,9 +208,9 @@ __global__ void __launch_bounds__(kPipeThreads, 2) decode_pipe_kernel(const __nv
 #pragma unroll
             for (int m = 0; m < kSweeps; ++m) {
                 const int r = r0 + kRowsPerPass * m;
-                const int j = key_at(st, r);
-                const bool ok = j >= 0;
-                const int64_t off = (int64_t)(ok ? j : 0) * row_stride + part * 8;
+                const int64_t row = key_row(key_at(st, r));
+                const bool ok = row >= 0;
+                const int64_t off = (ok ? row : 0) * row_stride + part * 8;
                 cp_async16(kt + sw_off(r, part), Kh + off, ok);
                 cp_async16(vt + sw_off(r, part), Vh + off, ok);
             }
@@ -375,17 +406,26 @@ __global__ void __launch_bounds__(D) decode_pipe_merge_kernel(int nsplit, const 
     if (lse && d == 0) lse[bh] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY;
 }
 
+// The kept lists and, for a paged cache, its geometry (block_table null: contiguous cache).
+struct PipeLists {
+    const int32_t* top_idx;
+    const int32_t* top_count;
+    int top_cap, window;
+    const int32_t* block_table;
+    int n_pages, max_pages, pshift;
+};
+
 template <int D>
 cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, int Lmax, const int32_t* cache_len,
-                         int H, int Hkv, const float* scores, const dma_kept_t* kept, float scale, void* o,
+                         int H, int Hkv, const float* scores, const PipeLists& kl, float scale, void* o,
                          float* lse, void* ws, int nsplit, int* status, cudaStream_t st)
 {
     PipeArgs a;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.cache_len = cache_len;
     a.scores = scores;
-    a.top_idx = kept->top_idx;
-    a.top_count = kept->top_count;
+    a.top_idx = kl.top_idx;
+    a.top_count = kl.top_count;
     a.part_o = static_cast<float*>(ws);
     a.part_ml = a.part_o + (size_t)B * H * nsplit * D;
     a.B = B;
@@ -393,17 +433,25 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     a.H = H;
     a.Hkv = Hkv;
     a.G = H / Hkv;
-    a.top_cap = kept->top_cap;
-    a.window = kept->window;
+    a.top_cap = kl.top_cap;
+    a.window = kl.window;
     a.nsplit = nsplit;
     a.c_log2 = scale * kLog2e;
+    a.block_table = kl.block_table;
+    a.n_pages = kl.n_pages;
+    a.max_pages = kl.max_pages;
+    a.pshift = kl.pshift;
+    a.status = status;
+    const bool paged = kl.block_table != nullptr;
     // the longest split's key list: ceil(stages / nsplit) stages of 64 keys
-    const int max_stages = std::max(1, (kept->top_cap + kept->window + kStageKeys - 1) / kStageKeys);
-    const int smem = PipeLayout<D>::smem_bytes(((max_stages + nsplit - 1) / nsplit) * kStageKeys);
-    cudaError_t e = cudaFuncSetAttribute(decode_pipe_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int max_stages = std::max(1, (kl.top_cap + kl.window + kStageKeys - 1) / kStageKeys);
+    const int smem = PipeLayout<D>::smem_bytes(((max_stages + nsplit - 1) / nsplit) * kStageKeys,
+                                               paged ? kl.max_pages : 0);
+    auto kernel = paged ? decode_pipe_kernel<D, true> : decode_pipe_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_pipe_kernel<D><<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(
-        static_cast<const __nv_bfloat16*>(Kc), static_cast<const __nv_bfloat16*>(Vc), a);
+    kernel<<<dim3(nsplit, B * Hkv), kPipeThreads, smem, st>>>(static_cast<const __nv_bfloat16*>(Kc),
+                                                              static_cast<const __nv_bfloat16*>(Vc), a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the merge launches while the partial kernel's last wave runs (programmatic dependent
     // launch), so the gap between the two kernels is hidden
@@ -419,6 +467,20 @@ cudaError_t launch_typed(const void* q, const void* Kc, const void* Vc, int B, i
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_pipe_merge_kernel<D>, nsplit, static_cast<const float*>(a.part_o),
                               static_cast<const float*>(a.part_ml), static_cast<__nv_bfloat16*>(o), lse);
+}
+
+cudaError_t launch_lists(const void* q, const void* Kc, const void* Vc, int B, int Lmax, const int32_t* cache_len,
+                         int H, int Hkv, int D, const float* scores, const PipeLists& kl, float scale, void* o,
+                         float* lse, void* ws, int* status, cudaStream_t st)
+{
+    // splits: the policy's, or more when a split's key list would not fit its shared-memory bound
+    const int max_stages = std::max(1, (kl.top_cap + kl.window + kStageKeys - 1) / kStageKeys);
+    const int nsplit = std::max(decode_pipe_splits(B, Hkv, kl.top_cap, kl.window),
+                                (max_stages * kStageKeys + kMaxSplitKeys - 1) / kMaxSplitKeys);
+    if (D == 128)
+        return launch_typed<128>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kl, scale, o, lse, ws, nsplit, status,
+                                 st);
+    return launch_typed<64>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kl, scale, o, lse, ws, nsplit, status, st);
 }
 
 }  // namespace
@@ -449,15 +511,19 @@ cudaError_t launch_decode_pipe(const void* q, const void* Kc, const void* Vc, in
                                const dma_kept_t* kept, float scale, void* o, float* lse, void* ws, int* status,
                                cudaStream_t st)
 {
-    // splits: the policy's, or more when a split's key list would not fit its shared-memory bound
-    const int max_stages = std::max(1, (kept->top_cap + kept->window + kStageKeys - 1) / kStageKeys);
-    const int nsplit = std::max(decode_pipe_splits(B, Hkv, kept->top_cap, kept->window),
-                                (max_stages * kStageKeys + kMaxSplitKeys - 1) / kMaxSplitKeys);
-    if (D == 128)
-        return launch_typed<128>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kept, scale, o, lse, ws, nsplit,
-                                 status, st);
-    return launch_typed<64>(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, scores, kept, scale, o, lse, ws, nsplit, status,
-                            st);
+    const PipeLists kl{kept->top_idx, kept->top_count, kept->top_cap, kept->window, nullptr, 0, 0, 0};
+    return launch_lists(q, Kc, Vc, B, Lmax, cache_len, H, Hkv, D, scores, kl, scale, o, lse, ws, status, st);
+}
+
+cudaError_t launch_decode_paged(const void* q, const void* Kp, const void* Vp, const int32_t* block_table,
+                                int n_pages, int B, int max_pages, int pshift, const int32_t* cache_len, int H,
+                                int Hkv, int D, const float* scores, const int32_t* top_idx,
+                                const int32_t* top_count, int top_cap, int window, float scale, void* o, float* lse,
+                                void* ws, int* status, cudaStream_t st)
+{
+    const PipeLists kl{top_idx, top_count, top_cap, window, block_table, n_pages, max_pages, pshift};
+    return launch_lists(q, Kp, Vp, B, max_pages << pshift, cache_len, H, Hkv, D, scores, kl, scale, o, lse, ws,
+                        status, st);
 }
 
 }  // namespace dma

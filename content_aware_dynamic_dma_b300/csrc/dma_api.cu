@@ -351,6 +351,105 @@ dma_status_t dma_sparse_attn_decode(const void* q, const void* Kc, const void* V
     return ok();
 }
 
+namespace {
+// page_size a power of two in [16, 128]: its log2, else -1
+int page_shift(int page_size)
+{
+    for (int s = 4; s <= 7; ++s)
+        if (page_size == (1 << s)) return s;
+    return -1;
+}
+}  // namespace
+
+dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                  int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                  int key_begin, int key_end, const float* W, const float* A, float* scores,
+                                  float* page_scores, dma_stream_t stream)
+{
+    const int ps = page_shift(page_size);
+    if (ps < 0) return fail(DMA_ERR_UNSUPPORTED, "page_size=%d (supported: 16, 32, 64, 128)", page_size);
+    if (max_pages < 1 || max_pages > 8192 || n_pages < 1)
+        return fail(DMA_ERR_INVALID_ARG, "max_pages=%d (1..8192) and n_pages=%d (>= 1)", max_pages, n_pages);
+    dma_status_t s = check_common(dt, B, max_pages * page_size, Hkv, D);
+    if (s != DMA_OK) return s;
+    if ((int64_t)n_pages * page_size * Hkv * D > ((int64_t)1 << 40)) return fail(DMA_ERR_UNSUPPORTED, "cache too large");
+    if (!V_pages || !block_table || !W || !scores)
+        return fail(DMA_ERR_INVALID_ARG, "V_pages, block_table, W and scores must be non-NULL");
+    if (!aligned16(V_pages) || !aligned4(block_table) || !aligned4(W) || !aligned4(scores) || (A && !aligned4(A)) ||
+        (page_scores && !aligned4(page_scores)) || (cache_len && !aligned4(cache_len)))
+        return fail(DMA_ERR_INVALID_ARG, "V_pages must be 16-byte aligned; the other arrays 4-byte aligned");
+    const int Lmax = max_pages * page_size;
+    if (key_begin < 0 || key_end < key_begin || key_end > Lmax)
+        return fail(DMA_ERR_INVALID_ARG, "key range [%d, %d) outside [0, %d]", key_begin, key_end, Lmax);
+    int* status = nullptr;
+    if ((s = status_ptr(&status)) != DMA_OK) return s;
+    cudaError_t e = launch_score_paged(V_pages, dt, block_table, n_pages, B, max_pages, ps, Hkv, D, key_begin, key_end,
+                                       cache_len, W, A, scores, page_scores, status,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged score launch");
+    return ok();
+}
+
+dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                              const int32_t* cache_len, int w, int32_t* top_idx, int32_t* top_count, int top_cap,
+                              dma_stream_t stream)
+{
+    const int ps = page_shift(page_size);
+    if (ps < 0) return fail(DMA_ERR_UNSUPPORTED, "page_size=%d (supported: 16, 32, 64, 128)", page_size);
+    if (B < 1 || Hkv < 1 || max_pages < 1 || max_pages > 8192 || w < 0)
+        return fail(DMA_ERR_INVALID_ARG, "B=%d Hkv=%d max_pages=%d (1..8192) w=%d", B, Hkv, max_pages, w);
+    if (!page_scores || !top_idx || !top_count)
+        return fail(DMA_ERR_INVALID_ARG, "page_scores, top_idx and top_count must be non-NULL");
+    if (!aligned4(page_scores) || !aligned4(top_idx) || !aligned4(top_count) || (cache_len && !aligned4(cache_len)))
+        return fail(DMA_ERR_INVALID_ARG, "arrays must be 4-byte aligned");
+    const int k_pages = w / page_size;
+    if (top_cap < k_pages * page_size)
+        return fail(DMA_ERR_INVALID_ARG, "top_cap=%d < floor(w / page_size) * page_size = %d", top_cap,
+                    k_pages * page_size);
+    cudaError_t e = launch_select_pages(page_scores, B, Hkv, max_pages, ps, cache_len, k_pages, top_idx, top_count,
+                                        top_cap, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "page selection launch");
+    return ok();
+}
+
+dma_status_t dma_sparse_attn_decode_paged(const void* q, const void* K_pages, const void* V_pages, dma_dtype_t dt,
+                                          int n_pages, const int32_t* block_table, int B, int max_pages,
+                                          int page_size, const int32_t* cache_len, int H, int Hkv, int D,
+                                          const float* scores, const int32_t* top_idx, const int32_t* top_count,
+                                          int top_cap, int window, float scale, void* o, float* lse, void* ws,
+                                          size_t ws_bytes, dma_stream_t stream)
+{
+    const int ps = page_shift(page_size);
+    if (ps < 0) return fail(DMA_ERR_UNSUPPORTED, "page_size=%d (supported: 16, 32, 64, 128)", page_size);
+    if (max_pages < 1 || max_pages > 8192 || n_pages < 1)
+        return fail(DMA_ERR_INVALID_ARG, "max_pages=%d (1..8192) and n_pages=%d (>= 1)", max_pages, n_pages);
+    dma_status_t s = check_common(dt, B, max_pages * page_size, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (H < 1 || H % Hkv != 0) return fail(DMA_ERR_INVALID_ARG, "H=%d must be a positive multiple of Hkv=%d", H, Hkv);
+    if (dt != DMA_BF16 || H / Hkv > 16)
+        return fail(DMA_ERR_UNSUPPORTED, "paged decode supports bf16 with up to 16 query heads per KV head");
+    if ((int64_t)n_pages * page_size * Hkv >= ((int64_t)1 << 31)) return fail(DMA_ERR_UNSUPPORTED, "cache too large");
+    if (top_cap < 0 || window < 0) return fail(DMA_ERR_INVALID_ARG, "top_cap=%d window=%d", top_cap, window);
+    if (!q || !K_pages || !V_pages || !block_table || !scores || !top_idx || !top_count || !o)
+        return fail(DMA_ERR_INVALID_ARG, "q, K_pages, V_pages, block_table, scores, top_idx, top_count, o non-NULL");
+    if (!aligned16(q) || !aligned16(K_pages) || !aligned16(V_pages) || !aligned16(o) || !aligned4(block_table) ||
+        !aligned4(scores) || !aligned4(top_idx) || !aligned4(top_count) || (lse && !aligned4(lse)) ||
+        (cache_len && !aligned4(cache_len)))
+        return fail(DMA_ERR_INVALID_ARG, "q, K_pages, V_pages, o must be 16-byte aligned; the rest 4-byte aligned");
+    const size_t need = decode_ws_bytes(B, H, Hkv, D, top_cap, window);
+    if (!ws || ws_bytes < need)
+        return fail(DMA_ERR_WORKSPACE, "decode workspace of %zu bytes given, %zu needed", ws ? ws_bytes : (size_t)0, need);
+    if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);
+    int* status = nullptr;
+    if ((s = status_ptr(&status)) != DMA_OK) return s;
+    cudaError_t e = launch_decode_paged(q, K_pages, V_pages, block_table, n_pages, B, max_pages, ps, cache_len, H, Hkv,
+                                        D, scores, top_idx, top_count, top_cap, window, scale, o, lse, ws, status,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+    return ok();
+}
+
 dma_status_t dma_backward_workspace_size(int B, int S, int H, int Hkv, int D, size_t* ws_bytes)
 {
     if (!ws_bytes) return fail(DMA_ERR_INVALID_ARG, "ws_bytes is NULL");

@@ -116,6 +116,20 @@ cudaError_t launch_score_bwd(const void* V, dma_dtype_t dt, int B, int S, int Hk
                              const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
                              cudaStream_t st);
 
+// Paged decode cache (K/V pages [n_pages][1 << pshift][Hkv][D], block_table [B][max_pages]).
+cudaError_t launch_score_paged(const void* Vp, dma_dtype_t dt, const int32_t* bt, int n_pages, int B, int max_pages,
+                               int pshift, int Hkv, int D, int key_begin, int key_end, const int32_t* cache_len,
+                               const float* W, const float* A, float* scores, float* page_scores, int* status,
+                               cudaStream_t st);
+cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int pshift,
+                                const int32_t* cache_len, int k_pages, int32_t* top_idx, int32_t* top_count,
+                                int top_cap, cudaStream_t st);
+cudaError_t launch_decode_paged(const void* q, const void* Kp, const void* Vp, const int32_t* block_table,
+                                int n_pages, int B, int max_pages, int pshift, const int32_t* cache_len, int H,
+                                int Hkv, int D, const float* scores, const int32_t* top_idx,
+                                const int32_t* top_count, int top_cap, int window, float scale, void* o, float* lse,
+                                void* ws, int* status, cudaStream_t st);
+
 size_t decode_ws_bytes(int B, int H, int Hkv, int D, int top_cap, int window);
 cudaError_t launch_decode(const void* q, const void* Kc, const void* Vc, dma_dtype_t dt, int B, int Lmax,
                           const int32_t* cache_len, int H, int Hkv, int D, const float* scores,

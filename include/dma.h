@@ -14,6 +14,8 @@
  *   dma_select_topk          per-key top-set intervals + per-query-tile key lists
  *   dma_sparse_attn_prefill  masked softmax attention over the kept keys
  *   dma_sparse_attn_decode   the same for one new query row per sequence
+ * plus page-granular decode over a paged KV cache (dma_score_keys_paged,
+ * dma_select_pages, dma_sparse_attn_decode_paged),
  * and two for the backward pass (training through the same mask):
  *   dma_sparse_attn_prefill_backward  dQ, dK, dV and ds over the kept pairs
  *   dma_score_keys_backward           ds -> dW, dA and the score's share of dV
@@ -215,6 +217,58 @@ dma_status_t dma_sparse_attn_decode_noalloc(const void* q, const void* Kc, const
                                             int Lmax, const int32_t* cache_len, int H, int Hkv, int D,
                                             const float* scores, const dma_kept_t* kept, float scale, void* o,
                                             float* lse, dma_stream_t stream);
+
+/* ----------------------------------------------------------- paged decode --
+ * Page-granular decode over a paged KV cache.  Sparse Frontier summary, decode
+ * findings: page-level (Quest) selection keeps the whole KV cache and picks pages
+ * of it; DMA summary §五/§七: the same content-derived scores and top-k rule.  A
+ * page's score is the maximum of its keys' scores (as for 64-key blocks); the
+ * decode row L-1 keeps the floor(w / page_size) complete pages (last key <= L-1)
+ * with the highest page scores, ties to the lower page index, united with the
+ * window {L-window .. L-1}.
+ *   K_pages, V_pages  device [n_pages][page_size][Hkv][D] (dtype dt)
+ *   block_table       device [B][max_pages] int32: logical page p of sequence b
+ *                     (keys p*page_size .. p*page_size+page_size-1) is physical
+ *                     page block_table[b][p]; entries for pages past cache_len
+ *                     are not read.  An entry outside [0, n_pages) is reported
+ *                     as DMA_ERR_DEVICE_CHECK and its rows are not read.
+ *   cache_len         device [B] int32 or NULL (= max_pages * page_size)
+ *   page_size         16, 32, 64 or 128;  1 <= max_pages <= 8192
+ * Scores are kept per logical position: scores [B][Hkv][max_pages * page_size],
+ * page_scores [B][Hkv][max_pages], both fp32.
+ */
+
+/* Scores of keys key_begin <= j < min(key_end, cache_len[b]) of every sequence
+ * (the dma_score_keys formula), read through the block table; when page_scores
+ * is non-NULL, also the page score of every page holding a key of
+ * [key_begin, key_end): the max over its keys below cache_len[b], whose scores
+ * must all be in `scores` (scored now or earlier). */
+dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                  int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                  int key_begin, int key_end, const float* W, const float* A, float* scores,
+                                  float* page_scores, dma_stream_t stream);
+
+/* The kept pages of every sequence's decode row, written as their keys:
+ *   top_idx    device [B][Hkv][top_cap] int32: the keys of the kept pages, ascending
+ *   top_count  device [B][Hkv] int32: their number
+ *   top_cap    >= floor(w / page_size) * page_size
+ * (the same top-set format as dma_kept_t.top_idx/top_count). */
+dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                              const int32_t* cache_len, int w, int32_t* top_idx, int32_t* top_count, int top_cap,
+                              dma_stream_t stream);
+
+/* Decode over the kept pages and the window (bf16 only; H / Hkv <= 16): the same
+ * result as dma_sparse_attn_decode over a contiguous cache holding the same rows.
+ *   q, o, lse, scale, ws  as for dma_sparse_attn_decode (ws of
+ *                         dma_decode_workspace_size(B, H, Hkv, D, top_cap, window))
+ *   scores                device [B][Hkv][max_pages * page_size] fp32
+ *   top_idx, top_count, top_cap  from dma_select_pages */
+dma_status_t dma_sparse_attn_decode_paged(const void* q, const void* K_pages, const void* V_pages, dma_dtype_t dt,
+                                          int n_pages, const int32_t* block_table, int B, int max_pages,
+                                          int page_size, const int32_t* cache_len, int H, int Hkv, int D,
+                                          const float* scores, const int32_t* top_idx, const int32_t* top_count,
+                                          int top_cap, int window, float scale, void* o, float* lse, void* ws,
+                                          size_t ws_bytes, dma_stream_t stream);
 
 /* --------------------------------------------------------------- backward --
  * DMA summary §四 (gradients flow through the top-k: kept positions get
