@@ -461,6 +461,67 @@ def bench_decode(args, world):
             "full_select_ms": full_ms, "full_select_keys": B * Hkv * L0}
 
 
+def bench_decode_paged(args, world, page_size=64):
+    """The decode workload over a paged cache (pages of `page_size` tokens in random physical
+    order): each step scores the new key and its page, selects the pages, and attends."""
+    import dataclasses
+    import content_aware_dynamic_dma_b300 as dma
+    cfg = wl.WORKLOADS[DECODE_WL]
+    if args.decode_batch != cfg.B:
+        cfg = dataclasses.replace(cfg, B=args.decode_batch)
+    B, L, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
+    n = args.steps
+    nq = args.warmup + n
+    d = wl.make_workload(cfg, n_queries=nq, device="cuda")
+    Kp, bt = wl.paginate(d.pop("Kc"), page_size, seed=cfg.seed)
+    Vp, _ = wl.paginate(d.pop("Vc"), page_size, seed=cfg.seed)
+    torch.cuda.empty_cache()
+    st = dma.PagedDecodeState(B, bt.shape[1], page_size, H, Hkv, D, cfg.w, cfg.window)
+    L0 = L - nq
+    stream = torch.cuda.current_stream()
+    st.full_score(Vp, bt, d["W"], cache_len=torch.full((B,), L0, dtype=torch.int32, device="cuda"))
+    o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    lens = [torch.full((B,), L0 + k + 1, dtype=torch.int32, device="cuda") for k in range(nq)]
+    j = torch.arange(st.top_cap, device="cuda")
+
+    def rows_kept(pos):
+        # kept rows per (b, KV head): keys of the kept pages outside the window, plus the window
+        tc = st.top_count.to(torch.int64)
+        valid = (j.view(1, 1, -1) < tc.unsqueeze(-1)) & (st.top_idx < pos + 1 - cfg.window)
+        return valid.sum() + B * Hkv * min(cfg.window, pos + 1)
+
+    for k in range(args.warmup):
+        st.step(d["q"][k], Kp, Vp, bt, d["W"], lens[k], L0 + k, o, lse, stream=stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    rows = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(n):
+        k = args.warmup + s
+        pos = L0 + k
+        ev[s][0].record(stream)
+        dma.dma_score_keys_paged(Vp, bt, d["W"], None, st.scores, st.page_scores, lens[k], pos, pos + 1,
+                                 stream=stream)
+        dma.dma_select_pages(st.page_scores, page_size, cfg.w, st.top_idx, st.top_count, lens[k], stream=stream)
+        ev[s][1].record(stream)
+        dma.dma_sparse_attn_decode_paged(d["q"][k], Kp, Vp, bt, st.scores, st.top_idx, st.top_count, cfg.window, o,
+                                         st.ws, lse, lens[k], stream=stream)
+        ev[s][2].record(stream)
+        rows.append(rows_kept(pos))
+    torch.cuda.synchronize()
+    barrier(world)
+    assert dma.dma_get_device_status() == 0
+    step_ms = max_over_ranks(sum(ev[s][0].elapsed_time(ev[s][2]) for s in range(n)), world) / n
+    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(n)]
+    sel_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(n)]
+    kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
+    return {"page_size": page_size, "gbs": sum(kv_bytes) / (sum(dec_ms) * 1e-3) / 1e9,
+            "decode_ms": statistics.mean(dec_ms), "score_and_select_pages_ms": statistics.mean(sel_ms),
+            "step_ms": step_ms, "selected_kv_bytes_per_step": statistics.mean(kv_bytes)}
+
+
 # ----------------------------------------------------------- CPU oracle -----
 
 def oracle_sample(cfg, n_rows: int, seed: int = 0, out=None):
@@ -653,6 +714,7 @@ def main():
             del p
             torch.cuda.empty_cache()
     dec = None if args.no_decode else bench_decode(args, world)
+    pdec = None if (args.no_decode or args.no_per_config) else bench_decode_paged(args, world)
     clk = clocks.stop()
 
     if rank != 0:
@@ -693,6 +755,13 @@ def main():
             "full_select_ms": round(dec["full_select_ms"], 4), "full_select_keys": dec["full_select_keys"],
             "decode_kernel_ms": round(dec["decode_ms"], 4), "decode_gbs": round(dec["gbs"], 2),
             "decode_frac_of_hbm": round(dec["gbs"] / peaks["hbm_gbs"], 4)}
+    if pdec is not None:
+        per_config[DECODE_WL + "_paged%d" % pdec["page_size"]] = {
+            "page_size": pdec["page_size"], "score_and_select_pages_ms": round(pdec["score_and_select_pages_ms"], 4),
+            "decode_kernel_ms": round(pdec["decode_ms"], 4), "decode_gbs": round(pdec["gbs"], 2),
+            "decode_frac_of_hbm": round(pdec["gbs"] / peaks["hbm_gbs"], 4), "step_ms": round(pdec["step_ms"], 4),
+            "selected_kv_bytes_per_step": pdec["selected_kv_bytes_per_step"],
+            "layout": "K/V pages [n_pages][page_size][Hkv][D] in random physical order behind a block table"}
     if per_config:
         line["per_config"] = per_config
     if not args.no_cpu_baseline and world == 1:

@@ -143,6 +143,26 @@ def make_grad(shape, dtype: torch.dtype, seed: int) -> torch.Tensor:
     return _randn(g, tuple(shape)).to(dtype).contiguous()
 
 
+def paginate(Kc: torch.Tensor, page_size: int, seed: int, extra_pages: int = 0):
+    """A paged copy of a contiguous cache Kc [B][L][Hkv][D]: pages [n_pages][page_size][Hkv][D]
+    with the physical pages in seeded random order (plus `extra_pages` unused ones), and the
+    block table [B][ceil(L / page_size)] int32; both on Kc's device."""
+    B, L, Hkv, D = Kc.shape
+    max_pages = (L + page_size - 1) // page_size
+    n_pages = B * max_pages + extra_pages
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(n_pages, generator=g)[:B * max_pages].view(B, max_pages)
+    pages = torch.zeros((n_pages, page_size, Hkv, D), dtype=Kc.dtype, device=Kc.device)
+    idx = perm.flatten().to(Kc.device)
+    if L == max_pages * page_size:
+        pages[idx] = Kc.reshape(B * max_pages, page_size, Hkv, D)
+    else:
+        pad = torch.zeros((B, max_pages * page_size, Hkv, D), dtype=Kc.dtype, device=Kc.device)
+        pad[:, :L] = Kc
+        pages[idx] = pad.view(B * max_pages, page_size, Hkv, D)
+    return pages.contiguous(), perm.to(torch.int32).to(Kc.device).contiguous()
+
+
 def make_workload(wl: Workload, n_queries: int = 1, device="cpu", batches=None):
     if wl.decode:
         return make_decode(wl.B, wl.S, wl.H, wl.Hkv, wl.D, wl.torch_dtype, wl.seed, wl.salient, n_queries,

@@ -29,18 +29,8 @@ def dma():
 
 
 def to_pages(Kc, page_size, seed, extra_pages=3):
-    """A paged copy of the contiguous cache Kc [B][L][Hkv][D]: pages in seeded random physical
-    order (plus unused pages); returns (pages [n_pages][page_size][Hkv][D], block_table int32)."""
-    B, L, Hkv, D = Kc.shape
-    max_pages = (L + page_size - 1) // page_size
-    n_pages = B * max_pages + extra_pages
-    g = torch.Generator().manual_seed(seed)
-    perm = torch.randperm(n_pages, generator=g)[:B * max_pages].view(B, max_pages)
-    pages = torch.zeros((n_pages, page_size, Hkv, D), dtype=Kc.dtype, device=Kc.device)
-    pad = torch.zeros((B, max_pages * page_size, Hkv, D), dtype=Kc.dtype, device=Kc.device)
-    pad[:, :L] = Kc
-    pages[perm.flatten().to(Kc.device)] = pad.view(B * max_pages, page_size, Hkv, D)
-    return pages.contiguous(), perm.to(torch.int32).to(Kc.device).contiguous()
+    """A paged copy of the contiguous cache (seeded random physical page order, spare pages)."""
+    return wl.paginate(Kc, page_size, seed, extra_pages)
 
 
 def run_paged(dma, d, page_size, w, window, lens, seed=3):
