@@ -9,8 +9,8 @@ it shares no code with the CUDA path: the arithmetic lives in ``dma_oracle.c``
 Functions (all take CPU torch tensors; floating inputs are widened to fp32
 exactly -- bf16 is a subset of fp32 -- and every result is fp64):
 
-* ``score(V, W, A)``            importance s = A_h * softplus(v . w_h)
-* ``select(scores, w, ...)``    per-key top-set interval end ("expiry")
+* ``score(V, W, A)``            importance s = A_h * softplus(v . w_h); form "exp": delta = e^s
+* ``select(scores, w, ...)``    per-key top-set interval end ("expiry"); w per KV head or one
 * ``attend_rows(...)``          dense masked softmax attention for listed rows
 * ``decode(...)``               the last row of a cache of length L
 * ``attend_backward(...)``      gradients through the kept pairs (dQ, dK, dV, d score)
@@ -82,30 +82,44 @@ def _ptr(a: Optional[np.ndarray]):
 
 
 def score(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor] = None, key_begin: int = 0,
-          key_end: Optional[int] = None) -> torch.Tensor:
+          key_end: Optional[int] = None, form: str = "log") -> torch.Tensor:
     """s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>), fp64 [B][Hkv][S].
 
-    Keys outside [key_begin, key_end) are left at 0.
+    form "exp" returns the dynamic weight itself, delta = exp(s) (DMA summary §五 writes
+    delta = exp(tau(v Delta) A)), for the variant that adds delta rather than log delta = s
+    to the logits.  Keys outside [key_begin, key_end) are left at 0.
     """
+    if form not in ("log", "exp"):
+        raise ValueError("form must be 'log' or 'exp'")
     B, S, Hkv, D = V.shape
     key_end = S if key_end is None else key_end
     v, w = _f32(V), _f32(W)
     a = None if A is None else _f32(A)
     out = np.zeros((B, Hkv, S), dtype=np.float64)
     _load().oracle_score(_ptr(v), _ptr(w), _ptr(a), B, S, Hkv, D, key_begin, key_end, _ptr(out))
+    if form == "exp":
+        out[:, :, key_begin:key_end] = np.exp(out[:, :, key_begin:key_end])
     return torch.from_numpy(out)
 
 
-def select(scores: torch.Tensor, w: int, block: int = 1, mode: int = ROWWISE) -> torch.Tensor:
+def select(scores: torch.Tensor, w, block: int = 1, mode: int = ROWWISE) -> torch.Tensor:
     """Per-key top-set interval end ("expiry"), int32 [B][Hkv][S].
 
     Key j is in the top set of rows lo_j <= i < expiry_j (lo_j = j for tokens,
     the block's last key for blocks); expiry_j = min(lo_j, S) means never.
+    w is one budget for every head, or a sequence of Hkv budgets (Sparse Frontier
+    summary, budget allocation across heads): KV head h of every sequence then
+    keeps w[h] keys, selected exactly as a uniform budget of w[h] on that head alone.
     """
     B, Hkv, S = scores.shape
+    if not isinstance(w, (int, np.integer)):
+        w = [int(x) for x in w]
+        if len(w) != Hkv:
+            raise ValueError("w needs one budget per KV head")
+        return torch.cat([select(scores[:, h:h + 1], w[h], block, mode) for h in range(Hkv)], dim=1)
     s = np.ascontiguousarray(scores.to(torch.float64).numpy())
     out = np.zeros((B, Hkv, S), dtype=np.int32)
-    _load().oracle_select(_ptr(s), B, Hkv, S, w, block, mode, _ptr(out))
+    _load().oracle_select(_ptr(s), B, Hkv, S, int(w), block, mode, _ptr(out))
     return torch.from_numpy(out)
 
 
@@ -129,23 +143,44 @@ def attend_rows(Q, K, V, scores, expiry, rows: Sequence[int], window: int, block
     return torch.from_numpy(O), torch.from_numpy(lse)
 
 
-def prefill(Q, K, V, W, A, w: int, window: int, block: int = 1, mode: int = ROWWISE, rows=None, scale=None):
-    """Score, select and attend in one call.  Returns (O, lse, scores, expiry)."""
+def prefill(Q, K, V, W, A, w, window: int, block: int = 1, mode: int = ROWWISE, rows=None, scale=None,
+            form: str = "log"):
+    """Score, select and attend in one call.  Returns (O, lse, scores, expiry); the selection
+    ranks the log-form scores, and form "exp" adds delta = e^s to the logits instead of s."""
     S = Q.shape[1]
     sc = score(V, W, A)
     ex = select(sc, w, block, mode)
+    bias = sc if form == "log" else score(V, W, A, form=form)
     rows = list(range(S)) if rows is None else rows
-    O, lse = attend_rows(Q, K, V, sc, ex, rows, window, block, scale)
+    O, lse = attend_rows(Q, K, V, bias, ex, rows, window, block, scale)
     return O, lse, sc, ex
 
 
-def decode(q, Kc, Vc, cache_len, scores, w: int, window: int, block: int = 1, mode: int = ROWWISE, scale=None):
+def decode(q, Kc, Vc, cache_len, scores, w, window: int, block: int = 1, mode: int = ROWWISE, scale=None,
+           bias=None):
     """Attention of one new query row per sequence over its cache of length
     cache_len[b].  q [B][H][D]; Kc, Vc [B][Lmax][Hkv][D]; scores fp64
-    [B][Hkv][Lmax].  Returns (o [B][H][D], lse [B][H]) in fp64."""
+    [B][Hkv][Lmax].  Returns (o [B][H][D], lse [B][H]) in fp64.
+
+    With per-head budgets (w a sequence) or a separate ``bias`` (the logits' bias, e.g. the
+    exp form delta, while ``scores`` ranks), each sequence is the last row of a prefill over
+    its own prefix: selection of that prefix, then attention of row L-1."""
     B, H, D = q.shape
     Lmax, Hkv = Kc.shape[1], Kc.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if bias is not None or not isinstance(w, (int, np.integer)):
+        bias = scores if bias is None else bias
+        o = torch.zeros((B, H, D), dtype=torch.float64)
+        lse = torch.zeros((B, H), dtype=torch.float64)
+        for b in range(B):
+            L = int(cache_len[b])
+            ex = select(scores[b:b + 1, :, :L], w, block, mode)
+            Qb = torch.zeros((1, L, H, D), dtype=torch.float32)
+            Qb[0, L - 1] = q[b].float()
+            ob, lb = attend_rows(Qb, Kc[b:b + 1, :L], Vc[b:b + 1, :L], bias[b:b + 1, :, :L], ex, [L - 1], window,
+                                 block, scale)
+            o[b], lse[b] = ob[0, 0], lb[0, :, 0]
+        return o, lse
     qq, k, v = _f32(q), _f32(Kc), _f32(Vc)
     cl = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int32))
     s = np.ascontiguousarray(scores.to(torch.float64).numpy())
@@ -184,12 +219,17 @@ def attend_backward(Q, K, V, scores, expiry, dO, window: int, block: int = 1, sc
     return torch.from_numpy(dQ), torch.from_numpy(dK), torch.from_numpy(dV), torch.from_numpy(ds)
 
 
-def score_backward(V, W, A, ds):
+def score_backward(V, W, A, ds, form: str = "log"):
     """Through s = A_h * softplus(v . w_h): returns (dV from the score [B][S][Hkv][D], dW [Hkv][D],
-    dA [Hkv]) in fp64, given ds = dL/ds [B][Hkv][S]."""
+    dA [Hkv]) in fp64, given ds = dL/ds [B][Hkv][S].  form "exp": ds is the gradient of the
+    added bias delta = exp(s), so dL/ds = ds * delta (chain rule) before the same steps."""
     B, S, Hkv, D = V.shape
     v, w = _f32(V), _f32(W)
     a = None if A is None else _f32(A)
+    if form == "exp":
+        ds = ds.to(torch.float64) * score(V, W, A, form="exp")
+    elif form != "log":
+        raise ValueError("form must be 'log' or 'exp'")
     g = np.ascontiguousarray(ds.to(torch.float64).numpy())
     dV = np.zeros((B, S, Hkv, D), dtype=np.float64)
     dW = np.zeros((Hkv, D), dtype=np.float64)
@@ -198,13 +238,16 @@ def score_backward(V, W, A, ds):
     return torch.from_numpy(dV), torch.from_numpy(dW), torch.from_numpy(dA)
 
 
-def backward(Q, K, V, W, A, w: int, window: int, dO, block: int = 1, mode: int = ROWWISE, scale=None):
+def backward(Q, K, V, W, A, w, window: int, dO, block: int = 1, mode: int = ROWWISE, scale=None,
+             form: str = "log"):
     """The whole backward of score -> select -> attend: returns (dQ, dK, dV, dW, dA) in fp64,
-    dV holding both the attention's and the score's part."""
+    dV holding both the attention's and the score's part.  The selection ranks s (form "exp"
+    adds delta = e^s to the logits: the same order, hence the same kept sets)."""
     sc = score(V, W, A)
     ex = select(sc, w, block, mode)
-    dQ, dK, dV, ds = attend_backward(Q, K, V, sc, ex, dO, window, block, scale)
-    dV2, dW, dA = score_backward(V, W, A, ds)
+    bias = sc if form == "log" else score(V, W, A, form=form)
+    dQ, dK, dV, ds = attend_backward(Q, K, V, bias, ex, dO, window, block, scale)
+    dV2, dW, dA = score_backward(V, W, A, ds, form)
     return dQ, dK, dV + dV2, dW, dA
 
 
@@ -224,18 +267,20 @@ def page_scores(scores, cache_len, page_size: int) -> torch.Tensor:
     return out
 
 
-def select_pages(scores, cache_len, page_size: int, w: int):
+def select_pages(scores, cache_len, page_size: int, w):
     """Kept pages of the decode row L-1 (L = cache_len[b]) for every (b, KV head): among the
     complete pages (last key <= L-1), the floor(w / page_size) with the highest page score,
     ties to the lower page index; scores compared as fp32 (-0 equals +0), as the selection
-    does.  Returns {(b, h): sorted list of kept page indices}."""
+    does.  w: one budget, or one per KV head.  Returns {(b, h): sorted list of kept page
+    indices}."""
     B, Hkv, _ = scores.shape
-    k = w // page_size
+    wh = [int(w)] * Hkv if isinstance(w, (int, np.integer)) else [int(x) for x in w]
     out = {}
     for b in range(B):
         L = int(cache_len[b])
         n_c = L // page_size
         for h in range(Hkv):
+            k = wh[h] // page_size
             vals = []
             for p in range(n_c):
                 v = max(float(np.float32(x)) + 0.0 for x in scores[b, h, p * page_size:(p + 1) * page_size].tolist())
