@@ -8,13 +8,16 @@ built, importing this package raises ImportError: there is no fallback.
 The functions carry the C names:
 
 * ``dma_score_keys``          s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>)
+* ``dma_score_keys_bias``     the same plus the logits' bias: s, or delta = exp(s)
 * ``dma_select_topk``         causal top-w selection (FULL or UPDATE)
+* ``dma_select_topk_heads``   the same with a budget per KV head
 * ``dma_sparse_attn_prefill`` masked softmax attention over the kept keys
 * ``dma_sparse_attn_decode``  the same for one new query row per sequence
 * ``dma_sparse_attn_prefill_backward``  dQ, dK, dV and ds over the kept pairs
 * ``dma_score_keys_backward``  ds -> dW, dA and the score's share of dV
-* ``dma_score_keys_paged``, ``dma_select_pages``, ``dma_sparse_attn_decode_paged``
-  page-granular decode over a paged KV cache
+  (``dma_score_keys_backward_bias``: for either form of the bias)
+* ``dma_score_keys_paged``, ``dma_select_pages`` (``dma_select_pages_heads``),
+  ``dma_sparse_attn_decode_paged``: page-granular decode over a paged KV cache
 
 plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and four
 compositions, ``prefill``, ``prefill_backward``, ``DecodeState`` and
@@ -45,6 +48,8 @@ ROWWISE = 0
 GLOBAL = 1
 FULL = 0
 UPDATE = 1
+BIAS_LOG = 0
+BIAS_EXP = 1
 Q_TILE = 128
 
 
@@ -68,7 +73,8 @@ EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_
             "dma_get_device_status", "dma_status_string", "dma_last_error_message", "dma_set_prefill_kernel",
             "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version", "dma_backward_workspace_size",
             "dma_sparse_attn_prefill_backward", "dma_score_keys_backward", "dma_score_keys_paged",
-            "dma_select_pages", "dma_sparse_attn_decode_paged")
+            "dma_select_pages", "dma_sparse_attn_decode_paged", "dma_score_keys_bias", "dma_select_topk_heads",
+            "dma_select_pages_heads", "dma_score_keys_backward_bias")
 
 
 def _load_lib():
@@ -99,6 +105,10 @@ def _load_lib():
         "dma_score_keys_paged": [P, I, I, P, I, I, I, P, I, I, I, I, P, P, P, P, P],
         "dma_select_pages": [P, I, I, I, I, P, I, P, P, I, P],
         "dma_sparse_attn_decode_paged": [P, P, P, I, I, P, I, I, I, P, I, I, I, P, P, P, I, I, F, P, P, P, Z, P],
+        "dma_score_keys_bias": [P, I, I, I, I, I, I, I, P, P, I, P, P, P],
+        "dma_select_topk_heads": [P, I, I, I, I, P, I, I, I, I, P, PK, P, Z, P],
+        "dma_select_pages_heads": [P, I, I, I, I, P, I, P, P, P, I, P],
+        "dma_score_keys_backward_bias": [P, I, I, I, I, I, P, P, I, P, P, P, P, P, Z, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -154,6 +164,16 @@ def dma_score_keys(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor], 
     key_end = S if key_end is None else key_end
     _check(_lib.dma_score_keys(_ptr(V), _dtype(V), B, S, Hkv, D, key_begin, key_end, _ptr(W), _ptr(A), _ptr(scores),
                                _stream(stream)))
+
+
+def dma_score_keys_bias(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor], form: int,
+                        scores: torch.Tensor, bias: torch.Tensor, key_begin: int = 0, key_end: Optional[int] = None,
+                        stream=None) -> None:
+    """scores (the ranking key s) and bias (s for BIAS_LOG, exp(s) for BIAS_EXP), [B][Hkv][S] fp32."""
+    B, S, Hkv, D = V.shape
+    key_end = S if key_end is None else key_end
+    _check(_lib.dma_score_keys_bias(_ptr(V), _dtype(V), B, S, Hkv, D, key_begin, key_end, _ptr(W), _ptr(A), form,
+                                    _ptr(scores), _ptr(bias), _stream(stream)))
 
 
 def dma_kept_layout(B: int, Hkv: int, S: int, w: int, window: int, block: int = 1, mode: int = ROWWISE):
@@ -221,6 +241,18 @@ def dma_select_topk(scores: torch.Tensor, kept: Kept, op: int = FULL, seq_len: O
     ws = kept.ws if ws is None else ws
     _check(_lib.dma_select_topk(_ptr(scores), B, Hkv, S, t.w, t.window, t.block, t.mode, op, _ptr(seq_len),
                                 ctypes.byref(t), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def dma_select_topk_heads(scores: torch.Tensor, kept: Kept, w_head: torch.Tensor, op: int = FULL,
+                          seq_len: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """w_head: device int32 [Hkv], 0 <= w_head[h] <= kept.w (the layout's budget)."""
+    B, Hkv, S = scores.shape
+    t = kept.t
+    ws = kept.ws if ws is None else ws
+    _check(_lib.dma_select_topk_heads(_ptr(scores), B, Hkv, S, t.w, _ptr(w_head), t.window, t.block, t.mode, op,
+                                      _ptr(seq_len), ctypes.byref(t), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream)))
 
 
 def dma_sparse_attn_prefill(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, scores: torch.Tensor, kept: Kept,
@@ -302,6 +334,18 @@ def dma_score_keys_backward(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.
                                         _stream(stream)))
 
 
+def dma_score_keys_backward_bias(V: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor], form: int,
+                                 ds: torch.Tensor, dV: torch.Tensor, dW: torch.Tensor,
+                                 dA: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                                 stream=None) -> None:
+    """dma_score_keys_backward for a bias of form BIAS_LOG or BIAS_EXP (ds = dL/d bias)."""
+    B, S, Hkv, D = V.shape
+    ws = _bwd_ws(ws, B, S, Hkv, Hkv, D, V.device)
+    _check(_lib.dma_score_keys_backward_bias(_ptr(V), _dtype(V), B, S, Hkv, D, _ptr(W), _ptr(A), form, _ptr(ds),
+                                             _ptr(dV), _ptr(dW), _ptr(dA), _ptr(ws), ws.numel() * ws.element_size(),
+                                             _stream(stream)))
+
+
 def dma_score_keys_paged(V_pages: torch.Tensor, block_table: torch.Tensor, W: torch.Tensor, A: Optional[torch.Tensor],
                          scores: torch.Tensor, page_scores: Optional[torch.Tensor] = None,
                          cache_len: Optional[torch.Tensor] = None, key_begin: int = 0, key_end: Optional[int] = None,
@@ -321,6 +365,15 @@ def dma_select_pages(page_scores: torch.Tensor, page_size: int, w: int, top_idx:
     B, Hkv, max_pages = page_scores.shape
     _check(_lib.dma_select_pages(_ptr(page_scores), B, Hkv, max_pages, page_size, _ptr(cache_len), w, _ptr(top_idx),
                                  _ptr(top_count), top_idx.shape[-1], _stream(stream)))
+
+
+def dma_select_pages_heads(page_scores: torch.Tensor, page_size: int, w: int, w_head: torch.Tensor,
+                           top_idx: torch.Tensor, top_count: torch.Tensor, cache_len: Optional[torch.Tensor] = None,
+                           stream=None) -> None:
+    B, Hkv, max_pages = page_scores.shape
+    _check(_lib.dma_select_pages_heads(_ptr(page_scores), B, Hkv, max_pages, page_size, _ptr(cache_len), w,
+                                       _ptr(w_head), _ptr(top_idx), _ptr(top_count), top_idx.shape[-1],
+                                       _stream(stream)))
 
 
 def dma_sparse_attn_decode_paged(q: torch.Tensor, K_pages: torch.Tensor, V_pages: torch.Tensor,
@@ -369,26 +422,40 @@ def dma_version() -> int:
 # ------------------------------------------------------------ compositions ---
 
 def prefill(Q, K, V, W, A, w: int, window: int, block: int = 1, mode: int = ROWWISE, scale: float = 0.0,
-            kept: Optional[Kept] = None, with_lse: bool = True, stream=None):
+            kept: Optional[Kept] = None, with_lse: bool = True, stream=None, form: int = BIAS_LOG,
+            w_head: Optional[torch.Tensor] = None):
     """Score, select and attend: the whole prefill hot path in three library calls.
 
-    Returns (O, lse, scores, kept)."""
+    form BIAS_EXP adds delta = exp(s) to the logits instead of s; w_head (device int32 [Hkv],
+    each at most w) gives every KV head its own budget.  Returns (O, lse, bias, kept): bias is
+    the array the logits got, which the backward and decode calls take as their scores --
+    the ranking scores themselves for BIAS_LOG."""
     B, S, H, D = Q.shape
     Hkv = K.shape[2]
     scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=Q.device)
-    dma_score_keys(V, W, A, scores, stream=stream)
+    bias = scores
+    if form == BIAS_LOG:
+        dma_score_keys(V, W, A, scores, stream=stream)
+    else:
+        bias = torch.empty_like(scores)
+        dma_score_keys_bias(V, W, A, form, scores, bias, stream=stream)
     if kept is None:
         kept = Kept(B, Hkv, S, w, window, block, mode, device=Q.device)
-    dma_select_topk(scores, kept, FULL, stream=stream)
+    if w_head is None:
+        dma_select_topk(scores, kept, FULL, stream=stream)
+    else:
+        dma_select_topk_heads(scores, kept, w_head, FULL, stream=stream)
     O = torch.empty_like(Q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=Q.device) if with_lse else None
-    dma_sparse_attn_prefill(Q, K, V, scores, kept, O, lse, scale, stream=stream)
-    return O, lse, scores, kept
+    dma_sparse_attn_prefill(Q, K, V, bias, kept, O, lse, scale, stream=stream)
+    return O, lse, bias, kept
 
 
-def prefill_backward(Q, K, V, W, A, O, lse, scores, kept: Kept, dO, scale: float = 0.0, stream=None):
-    """Backward of ``prefill`` through the same kept sets: returns (dQ, dK, dV, dW, dA), fp32,
-    with dV holding both the attention's and the score's share (dA is None when A is None)."""
+def prefill_backward(Q, K, V, W, A, O, lse, bias, kept: Kept, dO, scale: float = 0.0, stream=None,
+                     form: int = BIAS_LOG):
+    """Backward of ``prefill`` through the same kept sets (``bias`` as prefill returned it):
+    returns (dQ, dK, dV, dW, dA), fp32, with dV holding both the attention's and the score's
+    share (dA is None when A is None)."""
     B, S, H, D = Q.shape
     Hkv = K.shape[2]
     dev = Q.device
@@ -400,20 +467,40 @@ def prefill_backward(Q, K, V, W, A, O, lse, scores, kept: Kept, dO, scale: float
     dW = torch.empty((Hkv, D), **f32)
     dA = torch.empty((Hkv,), **f32) if A is not None else None
     ws = _bwd_ws(None, B, S, H, Hkv, D, dev)
-    dma_sparse_attn_prefill_backward(Q, K, V, scores, kept, O, lse, dO, dQ, dK, dV, ds, scale, ws, stream)
-    dma_score_keys_backward(V, W, A, ds, dV, dW, dA, ws, stream)
+    dma_sparse_attn_prefill_backward(Q, K, V, bias, kept, O, lse, dO, dQ, dK, dV, ds, scale, ws, stream)
+    if form == BIAS_LOG:
+        dma_score_keys_backward(V, W, A, ds, dV, dW, dA, ws, stream)
+    else:
+        dma_score_keys_backward_bias(V, W, A, form, ds, dV, dW, dA, ws, stream)
     return dQ, dK, dV, dW, dA
 
 
 class DecodeState:
-    """Decode-side buffers: the score cache, the kept top set and the workspace."""
+    """Decode-side buffers: the score cache, the kept top set and the workspace.  form BIAS_EXP
+    keeps a second cache, the bias delta = exp(s) the logits get; w_head (device int32 [Hkv],
+    each at most w) gives every KV head its own budget."""
 
-    def __init__(self, B: int, Lmax: int, H: int, Hkv: int, D: int, w: int, window: int, device="cuda"):
+    def __init__(self, B: int, Lmax: int, H: int, Hkv: int, D: int, w: int, window: int, device="cuda",
+                 form: int = BIAS_LOG, w_head: Optional[torch.Tensor] = None):
         self.B, self.Lmax, self.H, self.Hkv, self.D = B, Lmax, H, Hkv, D
+        self.form, self.w_head = form, w_head
         self.scores = torch.zeros((B, Hkv, Lmax), dtype=torch.float32, device=device)
+        self.bias = self.scores if form == BIAS_LOG else torch.zeros_like(self.scores)
         self.kept = Kept(B, Hkv, Lmax, w, window, 1, ROWWISE, device=device, tiles=False)
         self.ws = torch.empty((dma_decode_workspace_size(B, H, Hkv, D, self.kept.t.top_cap, window),),
                               dtype=torch.uint8, device=device)
+
+    def _score(self, Vc, W, A, key_begin, key_end, stream):
+        if self.form == BIAS_LOG:
+            dma_score_keys(Vc, W, A, self.scores, key_begin, key_end, stream=stream)
+        else:
+            dma_score_keys_bias(Vc, W, A, self.form, self.scores, self.bias, key_begin, key_end, stream=stream)
+
+    def _select(self, scores, kept, op, seq_len=None, stream=None):
+        if self.w_head is None:
+            dma_select_topk(scores, kept, op, seq_len=seq_len, stream=stream)
+        else:
+            dma_select_topk_heads(scores, kept, self.w_head, op, seq_len=seq_len, stream=stream)
 
     def full_select(self, Kc, Vc, W, A=None, length: Optional[int] = None, stream=None):
         """Scores the first ``length`` cache rows and selects the top set of row length-1.
@@ -422,24 +509,24 @@ class DecodeState:
         prefix selection included."""
         length = self.Lmax if length is None else length
         stream = torch.cuda.current_stream() if stream is None else stream
-        dma_score_keys(Vc, W, A, self.scores, 0, length, stream=stream)
+        self._score(Vc, W, A, 0, length, stream)
         if length == self.Lmax:
-            dma_select_topk(self.scores, self.kept, FULL, stream=stream)
+            self._select(self.scores, self.kept, FULL, stream=stream)
             return
         with torch.cuda.stream(stream):
             sub = Kept(self.B, self.Hkv, length, self.kept.w, self.kept.window, 1, ROWWISE,
                        device=self.scores.device, tiles=False)
             sc = self.scores[:, :, :length].contiguous()
-            dma_select_topk(sc, sub, FULL, stream=stream)
+            self._select(sc, sub, FULL, stream=stream)
             self.kept.top_idx[:, :, :sub.t.top_cap].copy_(sub.top_idx)
             self.kept.top_count.copy_(sub.top_count)
 
     def step(self, q, Kc, Vc, W, cache_len: torch.Tensor, new_pos: int, o, lse=None, A=None, scale: float = 0.0,
              stream=None):
         """One decode step for a token already appended at ``new_pos`` (= cache_len - 1)."""
-        dma_score_keys(Vc, W, A, self.scores, new_pos, new_pos + 1, stream=stream)
-        dma_select_topk(self.scores, self.kept, UPDATE, seq_len=cache_len, stream=stream)
-        dma_sparse_attn_decode(q, Kc, Vc, self.scores, self.kept, o, self.ws, lse, cache_len, scale, stream=stream)
+        self._score(Vc, W, A, new_pos, new_pos + 1, stream)
+        self._select(self.scores, self.kept, UPDATE, seq_len=cache_len, stream=stream)
+        dma_sparse_attn_decode(q, Kc, Vc, self.bias, self.kept, o, self.ws, lse, cache_len, scale, stream=stream)
 
 
 class PagedDecodeState:
@@ -447,9 +534,9 @@ class PagedDecodeState:
     the selected pages and the workspace."""
 
     def __init__(self, B: int, max_pages: int, page_size: int, H: int, Hkv: int, D: int, w: int, window: int,
-                 device="cuda"):
+                 device="cuda", w_head: Optional[torch.Tensor] = None):
         self.B, self.max_pages, self.page_size, self.H, self.Hkv, self.D = B, max_pages, page_size, H, Hkv, D
-        self.w, self.window = w, window
+        self.w, self.window, self.w_head = w, window, w_head
         f32 = dict(dtype=torch.float32, device=device)
         self.scores = torch.zeros((B, Hkv, max_pages * page_size), **f32)
         self.page_scores = torch.full((B, Hkv, max_pages), float("-inf"), **f32)
@@ -465,13 +552,21 @@ class PagedDecodeState:
         dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, 0, length,
                              stream=stream)
 
+    def select(self, cache_len=None, stream=None):
+        """The kept pages of every sequence's decode row, from the page scores."""
+        if self.w_head is None:
+            dma_select_pages(self.page_scores, self.page_size, self.w, self.top_idx, self.top_count, cache_len,
+                             stream=stream)
+        else:
+            dma_select_pages_heads(self.page_scores, self.page_size, self.w, self.w_head, self.top_idx,
+                                   self.top_count, cache_len, stream=stream)
+
     def step(self, q, K_pages, V_pages, block_table, W, cache_len: torch.Tensor, new_pos: int, o, lse=None, A=None,
              scale: float = 0.0, stream=None):
         """One decode step for a token already written at logical position ``new_pos``
         (= cache_len - 1): score it, update its page's score, select the pages, attend."""
         dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, new_pos,
                              new_pos + 1, stream=stream)
-        dma_select_pages(self.page_scores, self.page_size, self.w, self.top_idx, self.top_count, cache_len,
-                         stream=stream)
+        self.select(cache_len, stream)
         dma_sparse_attn_decode_paged(q, K_pages, V_pages, block_table, self.scores, self.top_idx, self.top_count,
                                      self.window, o, self.ws, lse, cache_len, scale, stream=stream)

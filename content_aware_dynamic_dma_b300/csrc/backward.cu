@@ -329,7 +329,7 @@ constexpr int kScoreBwdKeys = 256;
 template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads) score_bwd_kernel(const T* __restrict__ V, int S, int Hkv,
                                                                 const float* __restrict__ W,
-                                                                const float* __restrict__ A,
+                                                                const float* __restrict__ A, int exp_form,
                                                                 const float* __restrict__ ds, float* __restrict__ dV,
                                                                 float* __restrict__ part, int nchunk)
 {
@@ -357,10 +357,12 @@ __global__ void __launch_bounds__(kBwdThreads) score_bwd_kernel(const T* __restr
             u = fmaf(v[e], w[e], u);
         }
         u = warp_sum(u);
-        const float g = ds[((int64_t)b * Hkv + h) * S + j];
+        float g = ds[((int64_t)b * Hkv + h) * S + j];
         // softplus(u) = max(u, 0) + log1p(exp(-|u|)); sigmoid(u) = 1 / (1 + exp(-u))
         const float sp = fmaxf(u, 0.f) + log1pf(expf(-fabsf(u)));
         const float sg = 1.f / (1.f + expf(-u));
+        // exp form: ds is dL/d delta with delta = exp(s), so dL/ds = ds * delta
+        if (exp_form) g *= expf(gate * sp);
         const float du = g * gate * sg;
         da = fmaf(g, sp, da);
 #pragma unroll
@@ -424,13 +426,13 @@ cudaError_t simt_typed(const BwdArgs& a, cudaStream_t st)
 }
 
 template <typename T, int D>
-cudaError_t score_bwd_typed(const void* V, int B, int S, int Hkv, const float* W, const float* A, const float* ds,
-                            float* dV, float* dW, float* dA, float* part, cudaStream_t st)
+cudaError_t score_bwd_typed(const void* V, int B, int S, int Hkv, const float* W, const float* A, int exp_form,
+                            const float* ds, float* dV, float* dW, float* dA, float* part, cudaStream_t st)
 {
     const int nchunk = (S + kScoreBwdKeys - 1) / kScoreBwdKeys;
     dim3 grid(nchunk, Hkv, B);
-    score_bwd_kernel<T, D><<<grid, kBwdThreads, 0, st>>>(static_cast<const T*>(V), S, Hkv, W, A, ds, dV, part,
-                                                         nchunk);
+    score_bwd_kernel<T, D><<<grid, kBwdThreads, 0, st>>>(static_cast<const T*>(V), S, Hkv, W, A, exp_form, ds, dV,
+                                                         part, nchunk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n = Hkv * (D + 1);
@@ -462,16 +464,16 @@ cudaError_t launch_bwd_simt(const BwdArgs& a, dma_dtype_t dt, int D, cudaStream_
 }
 
 cudaError_t launch_score_bwd(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
-                             const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                             const float* A, int exp_form, const float* ds, float* dV, float* dW, float* dA, void* ws,
                              cudaStream_t st)
 {
     float* part = static_cast<float*>(ws);
     if (dt == DMA_BF16) {
-        if (D == 128) return score_bwd_typed<__nv_bfloat16, 128>(V, B, S, Hkv, W, A, ds, dV, dW, dA, part, st);
-        return score_bwd_typed<__nv_bfloat16, 64>(V, B, S, Hkv, W, A, ds, dV, dW, dA, part, st);
+        if (D == 128) return score_bwd_typed<__nv_bfloat16, 128>(V, B, S, Hkv, W, A, exp_form, ds, dV, dW, dA, part, st);
+        return score_bwd_typed<__nv_bfloat16, 64>(V, B, S, Hkv, W, A, exp_form, ds, dV, dW, dA, part, st);
     }
-    if (D == 128) return score_bwd_typed<float, 128>(V, B, S, Hkv, W, A, ds, dV, dW, dA, part, st);
-    return score_bwd_typed<float, 64>(V, B, S, Hkv, W, A, ds, dV, dW, dA, part, st);
+    if (D == 128) return score_bwd_typed<float, 128>(V, B, S, Hkv, W, A, exp_form, ds, dV, dW, dA, part, st);
+    return score_bwd_typed<float, 64>(V, B, S, Hkv, W, A, exp_form, ds, dV, dW, dA, part, st);
 }
 
 }  // namespace dma

@@ -186,20 +186,37 @@ dma_status_t dma_get_device_status(dma_stream_t stream, int* device_status)
     return ok();
 }
 
-dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
-                            const float* W, const float* A, float* scores, dma_stream_t stream)
+static dma_status_t score_impl(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
+                               int key_end, const float* W, const float* A, dma_bias_form_t form, float* scores,
+                               float* bias, dma_stream_t stream)
 {
     dma_status_t s = check_common(dt, B, S, Hkv, D);
     if (s != DMA_OK) return s;
     if (!V || !W || !scores) return fail(DMA_ERR_INVALID_ARG, "V, W and scores must be non-NULL");
-    if (!aligned16(V) || !aligned4(W) || !aligned4(scores) || (A && !aligned4(A)))
-        return fail(DMA_ERR_INVALID_ARG, "V must be 16-byte aligned; W, A, scores 4-byte aligned");
+    if (!aligned16(V) || !aligned4(W) || !aligned4(scores) || (A && !aligned4(A)) || (bias && !aligned4(bias)))
+        return fail(DMA_ERR_INVALID_ARG, "V must be 16-byte aligned; W, A, scores, bias 4-byte aligned");
+    if (form != DMA_BIAS_LOG && form != DMA_BIAS_EXP) return fail(DMA_ERR_INVALID_ARG, "form=%d", (int)form);
     if (key_begin < 0 || key_end < key_begin || key_end > S)
         return fail(DMA_ERR_INVALID_ARG, "key range [%d, %d) outside [0, %d]", key_begin, key_end, S);
-    cudaError_t e = launch_score(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, scores,
-                                 reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_score(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, scores, bias,
+                                 form == DMA_BIAS_EXP ? 1 : 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
     return ok();
+}
+
+dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
+                            const float* W, const float* A, float* scores, dma_stream_t stream)
+{
+    return score_impl(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, DMA_BIAS_LOG, scores, nullptr, stream);
+}
+
+dma_status_t dma_score_keys_bias(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
+                                 int key_end, const float* W, const float* A, dma_bias_form_t form, float* scores,
+                                 float* bias, dma_stream_t stream)
+{
+    if (!bias) return fail(DMA_ERR_INVALID_ARG, "bias is NULL (dma_score_keys writes the scores alone)");
+    if (bias == scores) return fail(DMA_ERR_INVALID_ARG, "bias and scores must be different arrays");
+    return score_impl(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, form, scores, bias, stream);
 }
 
 dma_status_t dma_kept_layout(int B, int Hkv, int S, int w, int window, int block, dma_sel_mode_t mode,
@@ -235,11 +252,12 @@ dma_status_t dma_kept_layout(int B, int Hkv, int S, int w, int window, int block
     return ok();
 }
 
-dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, int window, int block,
-                             dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len, dma_kept_t* kept, void* ws,
-                             size_t ws_bytes, dma_stream_t stream)
+static dma_status_t select_impl(const float* scores, int B, int Hkv, int S, int w, const int32_t* w_head, int window,
+                                int block, dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len,
+                                dma_kept_t* kept, void* ws, size_t ws_bytes, dma_stream_t stream)
 {
     if (!scores) return fail(DMA_ERR_INVALID_ARG, "scores is NULL");
+    if (w_head && !aligned4(w_head)) return fail(DMA_ERR_INVALID_ARG, "w_head must be 4-byte aligned");
     if (!aligned4(scores)) return fail(DMA_ERR_INVALID_ARG, "scores must be 4-byte aligned");
     dma_status_t s = check_kept_geometry(kept, B, Hkv, S);
     if (s != DMA_OK) return s;
@@ -255,7 +273,7 @@ dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, 
             return fail(DMA_ERR_UNSUPPORTED, "UPDATE supports budgets up to 51200 keys");
         if (seq_len && !aligned4(seq_len)) return fail(DMA_ERR_INVALID_ARG, "seq_len must be 4-byte aligned");
         if ((s = status_ptr(&status)) != DMA_OK) return s;
-        cudaError_t e = launch_select_update(scores, kept, seq_len, status, st);
+        cudaError_t e = launch_select_update(scores, kept, seq_len, w_head, status, st);
         if (e != cudaSuccess) return cuda_fail(e, "select update launch");
         return ok();
     }
@@ -274,9 +292,25 @@ dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, 
                     plan.bytes);
     if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
     if ((s = status_ptr(&status)) != DMA_OK) return s;
-    cudaError_t e = launch_select_full(scores, plan, kept, ws, status, st);
+    cudaError_t e = launch_select_full(scores, plan, kept, w_head, ws, status, st);
     if (e != cudaSuccess) return cuda_fail(e, "select launch");
     return ok();
+}
+
+dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, int window, int block,
+                             dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len, dma_kept_t* kept, void* ws,
+                             size_t ws_bytes, dma_stream_t stream)
+{
+    return select_impl(scores, B, Hkv, S, w, nullptr, window, block, mode, op, seq_len, kept, ws, ws_bytes, stream);
+}
+
+dma_status_t dma_select_topk_heads(const float* scores, int B, int Hkv, int S, int w, const int32_t* w_head,
+                                   int window, int block, dma_sel_mode_t mode, dma_sel_op_t op,
+                                   const int32_t* seq_len, dma_kept_t* kept, void* ws, size_t ws_bytes,
+                                   dma_stream_t stream)
+{
+    if (!w_head) return fail(DMA_ERR_INVALID_ARG, "w_head is NULL (dma_select_topk takes one budget)");
+    return select_impl(scores, B, Hkv, S, w, w_head, window, block, mode, op, seq_len, kept, ws, ws_bytes, stream);
 }
 
 dma_status_t dma_sparse_attn_prefill(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B, int S, int H,
@@ -390,9 +424,9 @@ dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pag
     return ok();
 }
 
-dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
-                              const int32_t* cache_len, int w, int32_t* top_idx, int32_t* top_count, int top_cap,
-                              dma_stream_t stream)
+static dma_status_t select_pages_impl(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                                      const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
+                                      int32_t* top_count, int top_cap, dma_stream_t stream)
 {
     const int ps = page_shift(page_size);
     if (ps < 0) return fail(DMA_ERR_UNSUPPORTED, "page_size=%d (supported: 16, 32, 64, 128)", page_size);
@@ -400,16 +434,37 @@ dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_
         return fail(DMA_ERR_INVALID_ARG, "B=%d Hkv=%d max_pages=%d (1..8192) w=%d", B, Hkv, max_pages, w);
     if (!page_scores || !top_idx || !top_count)
         return fail(DMA_ERR_INVALID_ARG, "page_scores, top_idx and top_count must be non-NULL");
-    if (!aligned4(page_scores) || !aligned4(top_idx) || !aligned4(top_count) || (cache_len && !aligned4(cache_len)))
+    if (!aligned4(page_scores) || !aligned4(top_idx) || !aligned4(top_count) || (cache_len && !aligned4(cache_len)) ||
+        (w_head && !aligned4(w_head)))
         return fail(DMA_ERR_INVALID_ARG, "arrays must be 4-byte aligned");
     const int k_pages = w / page_size;
     if (top_cap < k_pages * page_size)
         return fail(DMA_ERR_INVALID_ARG, "top_cap=%d < floor(w / page_size) * page_size = %d", top_cap,
                     k_pages * page_size);
-    cudaError_t e = launch_select_pages(page_scores, B, Hkv, max_pages, ps, cache_len, k_pages, top_idx, top_count,
-                                        top_cap, reinterpret_cast<cudaStream_t>(stream));
+    int* status = nullptr;
+    dma_status_t s;
+    if (w_head && (s = status_ptr(&status)) != DMA_OK) return s;
+    cudaError_t e = launch_select_pages(page_scores, B, Hkv, max_pages, ps, cache_len, w, w_head, top_idx, top_count,
+                                        top_cap, status, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "page selection launch");
     return ok();
+}
+
+dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                              const int32_t* cache_len, int w, int32_t* top_idx, int32_t* top_count, int top_cap,
+                              dma_stream_t stream)
+{
+    return select_pages_impl(page_scores, B, Hkv, max_pages, page_size, cache_len, w, nullptr, top_idx, top_count,
+                             top_cap, stream);
+}
+
+dma_status_t dma_select_pages_heads(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                                    const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
+                                    int32_t* top_count, int top_cap, dma_stream_t stream)
+{
+    if (!w_head) return fail(DMA_ERR_INVALID_ARG, "w_head is NULL (dma_select_pages takes one budget)");
+    return select_pages_impl(page_scores, B, Hkv, max_pages, page_size, cache_len, w, w_head, top_idx, top_count,
+                             top_cap, stream);
 }
 
 dma_status_t dma_sparse_attn_decode_paged(const void* q, const void* K_pages, const void* V_pages, dma_dtype_t dt,
@@ -521,10 +576,11 @@ dma_status_t dma_sparse_attn_prefill_backward(const void* Q, const void* K, cons
     return ok();
 }
 
-dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
-                                     const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
-                                     size_t ws_bytes, dma_stream_t stream)
+static dma_status_t score_backward_impl(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
+                                        const float* A, dma_bias_form_t form, const float* ds, float* dV, float* dW,
+                                        float* dA, void* ws, size_t ws_bytes, dma_stream_t stream)
 {
+    if (form != DMA_BIAS_LOG && form != DMA_BIAS_EXP) return fail(DMA_ERR_INVALID_ARG, "form=%d", (int)form);
     dma_status_t s = check_common(dt, B, S, Hkv, D);
     if (s != DMA_OK) return s;
     if (!V || !W || !ds || !dV || !dW) return fail(DMA_ERR_INVALID_ARG, "V, W, ds, dV and dW must be non-NULL");
@@ -536,9 +592,25 @@ dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S
         return fail(DMA_ERR_WORKSPACE, "score backward workspace of %zu bytes given, %zu needed",
                     ws ? ws_bytes : (size_t)0, need);
     if (!aligned16(ws)) return fail(DMA_ERR_WORKSPACE, "workspace must be 16-byte aligned");
-    cudaError_t e = launch_score_bwd(V, dt, B, S, Hkv, D, W, A, ds, dV, dW, dA, ws, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_score_bwd(V, dt, B, S, Hkv, D, W, A, form == DMA_BIAS_EXP ? 1 : 0, ds, dV, dW, dA, ws,
+                                     reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score backward launch");
     return ok();
+}
+
+dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
+                                     const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                                     size_t ws_bytes, dma_stream_t stream)
+{
+    return score_backward_impl(V, dt, B, S, Hkv, D, W, A, DMA_BIAS_LOG, ds, dV, dW, dA, ws, ws_bytes, stream);
+}
+
+dma_status_t dma_score_keys_backward_bias(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D,
+                                          const float* W, const float* A, dma_bias_form_t form, const float* ds,
+                                          float* dV, float* dW, float* dA, void* ws, size_t ws_bytes,
+                                          dma_stream_t stream)
+{
+    return score_backward_impl(V, dt, B, S, Hkv, D, W, A, form, ds, dV, dW, dA, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -58,12 +58,12 @@ dma_status_t set_error(dma_status_t s, const char* fmt, ...);
 // ---- launchers (host) -----------------------------------------------------
 
 cudaError_t launch_score(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
-                         const float* W, const float* A, float* scores, cudaStream_t st);
+                         const float* W, const float* A, float* scores, float* bias, int exp_form, cudaStream_t st);
 
-cudaError_t launch_select_full(const float* scores, const SelectPlan& plan, const dma_kept_t* kept, void* ws,
-                               int* status, cudaStream_t st);
-cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len, int* status,
-                                 cudaStream_t st);
+cudaError_t launch_select_full(const float* scores, const SelectPlan& plan, const dma_kept_t* kept,
+                               const int32_t* w_head, void* ws, int* status, cudaStream_t st);
+cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len,
+                                 const int32_t* w_head, int* status, cudaStream_t st);
 
 cudaError_t launch_prefill_simt(const void* Q, const void* K, const void* V, dma_dtype_t dt, int B, int S, int H,
                                 int Hkv, int D, const float* scores, const dma_kept_t* kept, float scale, void* O,
@@ -113,7 +113,7 @@ cudaError_t launch_bwd_simt(const BwdArgs& a, dma_dtype_t dt, int D, cudaStream_
 bool bwd_tc_supported(dma_dtype_t dt, int D);
 cudaError_t launch_bwd_tc(const BwdArgs& a, int D, uint64_t wait_ns, cudaStream_t st);
 cudaError_t launch_score_bwd(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
-                             const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
+                             const float* A, int exp_form, const float* ds, float* dV, float* dW, float* dA, void* ws,
                              cudaStream_t st);
 
 // Paged decode cache (K/V pages [n_pages][1 << pshift][Hkv][D], block_table [B][max_pages]).
@@ -122,8 +122,8 @@ cudaError_t launch_score_paged(const void* Vp, dma_dtype_t dt, const int32_t* bt
                                const float* W, const float* A, float* scores, float* page_scores, int* status,
                                cudaStream_t st);
 cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int pshift,
-                                const int32_t* cache_len, int k_pages, int32_t* top_idx, int32_t* top_count,
-                                int top_cap, cudaStream_t st);
+                                const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
+                                int32_t* top_count, int top_cap, int* status, cudaStream_t st);
 cudaError_t launch_decode_paged(const void* q, const void* Kp, const void* Vp, const int32_t* block_table,
                                 int n_pages, int B, int max_pages, int pshift, const int32_t* cache_len, int H,
                                 int Hkv, int D, const float* scores, const int32_t* top_idx,

@@ -144,18 +144,30 @@ __device__ void bitonic_sort(unsigned long long* keys, int n)
 }
 
 // The kept pages of the decode row of one (b, h) segment, written as their keys (ascending).
+// The budget is w keys, or w_head[h] (clamped into [0, w], an entry outside recorded) when
+// given: floor(budget / page size) pages.
 __global__ void __launch_bounds__(kSelectThreads) select_pages_kernel(const float* __restrict__ page_scores,
                                                                       const int32_t* __restrict__ cache_len, int Hkv,
-                                                                      int max_pages, int pshift, int k_pages,
+                                                                      int max_pages, int pshift, int w,
+                                                                      const int32_t* __restrict__ w_head,
                                                                       int32_t* __restrict__ top_idx,
-                                                                      int32_t* __restrict__ top_count, int top_cap)
+                                                                      int32_t* __restrict__ top_count, int top_cap,
+                                                                      int* status)
 {
     extern __shared__ unsigned long long keys[];  // [pow2 >= complete pages]
     const int seg = blockIdx.x, b = seg / Hkv;
     const int Lmax = max_pages << pshift;
     const int L = cache_len ? min(max(cache_len[b], 0), Lmax) : Lmax;
     const int n_c = min(L >> pshift, max_pages);  // complete pages
-    const int k = min(k_pages, n_c);
+    int wb = w;
+    if (w_head) {
+        wb = w_head[seg % Hkv];
+        if (wb < 0 || wb > w) {
+            if (threadIdx.x == 0) set_status(status, DMA_ERR_DEVICE_CHECK);
+            wb = wb < 0 ? 0 : w;
+        }
+    }
+    const int k = min(wb >> pshift, n_c);
     const float* ps = page_scores + (int64_t)seg * max_pages;
     const int P = 1 << pshift;
     if (k < n_c) {
@@ -220,8 +232,8 @@ cudaError_t launch_score_paged(const void* Vp, dma_dtype_t dt, const int32_t* bt
 }
 
 cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int pshift,
-                                const int32_t* cache_len, int k_pages, int32_t* top_idx, int32_t* top_count,
-                                int top_cap, cudaStream_t st)
+                                const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
+                                int32_t* top_count, int top_cap, int* status, cudaStream_t st)
 {
     int n = 1;
     while (n < max_pages) n <<= 1;
@@ -231,8 +243,8 @@ cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int ma
         (e = cudaFuncSetAttribute(select_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
             cudaSuccess)
         return e;
-    select_pages_kernel<<<B * Hkv, kSelectThreads, smem, st>>>(page_scores, cache_len, Hkv, max_pages, pshift, k_pages,
-                                                               top_idx, top_count, top_cap);
+    select_pages_kernel<<<B * Hkv, kSelectThreads, smem, st>>>(page_scores, cache_len, Hkv, max_pages, pshift, w,
+                                                               w_head, top_idx, top_count, top_cap, status);
     return cudaGetLastError();
 }
 

@@ -4,8 +4,13 @@
 // delta = exp(tau(v Delta) * A) with tau non-negative; its logarithm, with tau =
 // softplus, a per-KV-head vector Delta = W[h] and gate A_h, is the score.
 //
+// With a bias array, the kernel also writes the value the logits get: s itself,
+// or (exp form) delta = exp(s), the dynamic weight as the summary writes it.  The
+// selection ranks s either way: exp is increasing, so the kept sets are those of
+// delta, without the ties that rounding large delta to fp32 would add.
+//
 // HBM-bound: every value row is read once (D * elem bytes) and 4 bytes are
-// written per (key, head).  The rows of TJ consecutive keys and all Hkv heads are
+// written per (key, head) and output array.  The rows of TJ consecutive keys and all Hkv heads are
 // one contiguous span of V, so a CTA streams that span with 16-byte loads, each
 // row reduced by the CPR lanes that hold it, and writes the TJ scores of each
 // head as one coalesced run.
@@ -20,7 +25,8 @@ constexpr int kScoreTJ = 32;  // keys per CTA
 template <typename T, int D>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restrict__ V, int S, int Hkv, int key_begin,
                                                               int key_end, const float* __restrict__ W,
-                                                              const float* __restrict__ A, float* __restrict__ out)
+                                                              const float* __restrict__ A, float* __restrict__ out,
+                                                              float* __restrict__ bias, int exp_form)
 {
     constexpr int kElem = 16 / sizeof(T);    // elements per 16-byte chunk
     constexpr int kCPR = D / kElem;          // chunks per row (8..32)
@@ -75,13 +81,17 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
     __syncthreads();
     for (int t = threadIdx.x; t < Hkv * kScoreTJ; t += kScoreThreads) {
         int h = t / kScoreTJ, jj = t % kScoreTJ;
-        if (jj < nj) out[((int64_t)b * Hkv + h) * S + j0 + jj] = s_s[t];
+        if (jj < nj) {
+            const int64_t o = ((int64_t)b * Hkv + h) * S + j0 + jj;
+            out[o] = s_s[t];
+            if (bias) bias[o] = exp_form ? expf(s_s[t]) : s_s[t];
+        }
     }
 }
 
 template <typename T, int D>
 cudaError_t launch_typed(const void* V, int B, int S, int Hkv, int key_begin, int key_end, const float* W,
-                         const float* A, float* scores, cudaStream_t st)
+                         const float* A, float* scores, float* bias, int exp_form, cudaStream_t st)
 {
     dim3 grid((key_end - key_begin + kScoreTJ - 1) / kScoreTJ, B);
     size_t smem = sizeof(float) * (size_t)Hkv * (D + kScoreTJ);
@@ -91,22 +101,23 @@ cudaError_t launch_typed(const void* V, int B, int S, int Hkv, int key_begin, in
         if (e != cudaSuccess) return e;
     }
     score_kernel<T, D><<<grid, kScoreThreads, smem, st>>>(static_cast<const T*>(V), S, Hkv, key_begin, key_end, W,
-                                                          A, scores);
+                                                          A, scores, bias, exp_form);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_score(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
-                         const float* W, const float* A, float* scores, cudaStream_t st)
+                         const float* W, const float* A, float* scores, float* bias, int exp_form, cudaStream_t st)
 {
     if (key_end <= key_begin) return cudaSuccess;
     if (dt == DMA_BF16) {
-        if (D == 128) return launch_typed<__nv_bfloat16, 128>(V, B, S, Hkv, key_begin, key_end, W, A, scores, st);
-        return launch_typed<__nv_bfloat16, 64>(V, B, S, Hkv, key_begin, key_end, W, A, scores, st);
+        if (D == 128)
+            return launch_typed<__nv_bfloat16, 128>(V, B, S, Hkv, key_begin, key_end, W, A, scores, bias, exp_form, st);
+        return launch_typed<__nv_bfloat16, 64>(V, B, S, Hkv, key_begin, key_end, W, A, scores, bias, exp_form, st);
     }
-    if (D == 128) return launch_typed<float, 128>(V, B, S, Hkv, key_begin, key_end, W, A, scores, st);
-    return launch_typed<float, 64>(V, B, S, Hkv, key_begin, key_end, W, A, scores, st);
+    if (D == 128) return launch_typed<float, 128>(V, B, S, Hkv, key_begin, key_end, W, A, scores, bias, exp_form, st);
+    return launch_typed<float, 64>(V, B, S, Hkv, key_begin, key_end, W, A, scores, bias, exp_form, st);
 }
 
 }  // namespace dma

@@ -276,11 +276,36 @@ __global__ void __launch_bounds__(kRadixThreads) radix_scatter_kernel(RadixIn in
     }
 }
 
+// ------------------------------------------------------------ unit budget --
+
+// The budget in units of one segment (b, KV head h).  Uniform: k_max.  Per head
+// (Sparse Frontier summary, budget allocation across heads): w_head[h] keys,
+// floor(w_head[h] / block) units; an entry outside [0, w_max] -- the budget the
+// kept layout was sized for -- is recorded and clamped into that range.
+struct HeadBudget {
+    const int32_t* w_head;  // device [Hkv] or nullptr
+    int Hkv, block, w_max, k_max;
+};
+
+__device__ __forceinline__ int seg_budget(const HeadBudget& hb, int seg, int* status, bool report)
+{
+    if (!hb.w_head) return hb.k_max;
+    int w = hb.w_head[seg % hb.Hkv];
+    if (w < 0 || w > hb.w_max) {
+        if (report) set_status(status, DMA_ERR_DEVICE_CHECK);
+        w = w < 0 ? 0 : hb.w_max;
+    }
+    const int k = hb.block > 1 ? w / hb.block : w;
+    return k < hb.k_max ? k : hb.k_max;
+}
+
 // ------------------------------------------------------------ expiry (global) --
 
-__global__ void global_expiry_kernel(const int32_t* __restrict__ rank, int n, int k, int32_t* __restrict__ E)
+__global__ void global_expiry_kernel(const int32_t* __restrict__ rank, int n, HeadBudget hb,
+                                     int32_t* __restrict__ E, int* status)
 {
     const int seg = blockIdx.y;
+    const int k = seg_budget(hb, seg, status, blockIdx.x == 0 && threadIdx.x == 0);
     const int u = blockIdx.x * blockDim.x + threadIdx.x;
     if (u < n) E[(int64_t)seg * n + u] = rank[(int64_t)seg * n + u] < k ? n : u;
 }
@@ -360,14 +385,15 @@ __device__ int block_exclusive_scan(int v, int* warp_buf, int* total)
 constexpr int kBoundaryThreads = 256;
 __global__ void __launch_bounds__(kBoundaryThreads) boundary_kernel(const int32_t* __restrict__ p,
                                                                    const int32_t* __restrict__ rank,
-                                                                   const int32_t* __restrict__ tab, int n, int k,
-                                                                   int T, int nC, int X, int nX,
+                                                                   const int32_t* __restrict__ tab, int n,
+                                                                   HeadBudget hb, int T, int nC, int X, int nX,
                                                                    int32_t* __restrict__ f0, int* status)
 {
     extern __shared__ int32_t cnt[];  // [nX]
     __shared__ int warp_buf[32];
     __shared__ int sel_block, sel_need;
     const int seg = blockIdx.y, c = blockIdx.x;
+    const int k = seg_budget(hb, seg, status, c == 0 && threadIdx.x == 0);
     const int t_begin = c * T, t_end = min(n, t_begin + T);
     const int t_start = max(t_begin, k);
     if (t_start >= t_end) return;
@@ -433,7 +459,7 @@ constexpr int kWalkWarps = 4;
 constexpr int kWalkSmemWarps = 32;
 template <bool kSmem>
 __global__ void walk_kernel(const int32_t* __restrict__ p, const int32_t* __restrict__ rank,
-                            const int32_t* __restrict__ f0, int nseg, int n, int k, int T, int nC,
+                            const int32_t* __restrict__ f0, int nseg, int n, HeadBudget hb, int T, int nC,
                             int32_t* __restrict__ E, int* status)
 {
     extern __shared__ uint16_t rk16[];  // [n] (kSmem)
@@ -452,6 +478,7 @@ __global__ void walk_kernel(const int32_t* __restrict__ p, const int32_t* __rest
         seg = gw / nC;
         c = gw % nC;
     }
+    const int k = seg_budget(hb, seg, status, false);  // reported by the boundary kernel
     const int32_t* ps = p + (int64_t)seg * n;
     const int32_t* rs = rank + (int64_t)seg * n;
     auto rank_at = [&](int pos) -> int { return kSmem ? (int)rk16[pos] : rs[pos]; };
@@ -1004,7 +1031,7 @@ __global__ void __launch_bounds__(kUpdateThreads) update_kernel(const float* __r
                                                                 const int32_t* __restrict__ seq_len,
                                                                 int32_t* __restrict__ top_idx,
                                                                 int32_t* __restrict__ top_count, int top_cap,
-                                                                int budget, int* status)
+                                                                HeadBudget hb, int* status)
 {
     extern __shared__ int32_t buf[];  // [budget]
     __shared__ uint32_t red_key[32];
@@ -1012,6 +1039,7 @@ __global__ void __launch_bounds__(kUpdateThreads) update_kernel(const float* __r
     __shared__ int worst_pos;
     const int seg = blockIdx.x;
     const int b = seg / Hkv;
+    const int budget = seg_budget(hb, seg, status, threadIdx.x == 0);
     const int t = seq_len ? seq_len[b] - 1 : S - 1;
     const float* sc = scores + (int64_t)seg * S;
     int32_t* ti = top_idx + (int64_t)seg * top_cap;
@@ -1131,8 +1159,8 @@ SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block)
     return pl;
 }
 
-cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const dma_kept_t* kept, void* ws,
-                               int* status, cudaStream_t st)
+cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const dma_kept_t* kept,
+                               const int32_t* w_head, void* ws, int* status, cudaStream_t st)
 {
     char* W = static_cast<char*>(ws);
     const int nseg = pl.nseg, n = pl.n, S = pl.S, block = kept->block;
@@ -1146,6 +1174,7 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
     int32_t* bexp = reinterpret_cast<int32_t*>(W + pl.off_bexp);
     cudaError_t e;
 
+    const HeadBudget hb{w_head, kept->Hkv, block, kept->w, pl.k};
     const float* unit_values = scores;
     int32_t* E = kept->expiry;  // token units: the unit expiry is the key expiry
     if (block > 1) {
@@ -1180,11 +1209,11 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
         const int32_t* p = valb[1];
         // 2-3. unit expiry
         if (kept->mode == DMA_SEL_GLOBAL) {
-            global_expiry_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(rank, n, pl.k, E);
+            global_expiry_kernel<<<dim3((n + 255) / 256, nseg), 256, 0, st>>>(rank, n, hb, E, status);
         } else {
             count_table_kernel<<<dim3(pl.nC, nseg), 256, pl.nX * 4, st>>>(p, n, pl.T, pl.nC, pl.X, pl.nX, tab);
             count_prefix_kernel<<<dim3((pl.nX + 127) / 128, nseg), 128, 0, st>>>(tab, pl.nC, pl.nX);
-            boundary_kernel<<<dim3(pl.nC, nseg), kBoundaryThreads, pl.nX * 4, st>>>(p, rank, tab, n, pl.k, pl.T,
+            boundary_kernel<<<dim3(pl.nC, nseg), kBoundaryThreads, pl.nX * 4, st>>>(p, rank, tab, n, hb, pl.T,
                                                                                     pl.nC, pl.X, pl.nX, f0, status);
             if (n <= 65536) {
                 const int smem = n * 2;
@@ -1193,11 +1222,11 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
                         cudaSuccess)
                     return e;
                 walk_kernel<true><<<dim3((pl.nC + kWalkSmemWarps - 1) / kWalkSmemWarps, nseg), kWalkSmemWarps * 32,
-                                    smem, st>>>(p, rank, f0, nseg, n, pl.k, pl.T, pl.nC, E, status);
+                                    smem, st>>>(p, rank, f0, nseg, n, hb, pl.T, pl.nC, E, status);
             } else {
                 const int walkers = nseg * pl.nC;
                 walk_kernel<false><<<(walkers + kWalkWarps - 1) / kWalkWarps, kWalkWarps * 32, 0, st>>>(
-                    p, rank, f0, nseg, n, pl.k, pl.T, pl.nC, E, status);
+                    p, rank, f0, nseg, n, hb, pl.T, pl.nC, E, status);
             }
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -1236,18 +1265,19 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
     return cudaSuccess;
 }
 
-cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len, int* status,
-                                 cudaStream_t st)
+cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len,
+                                 const int32_t* w_head, int* status, cudaStream_t st)
 {
     const int nseg = kept->B * kept->Hkv;
     const int budget = kept->w < kept->S ? kept->w : kept->S;
+    const HeadBudget hb{w_head, kept->Hkv, 1, kept->w, budget};
     size_t smem = (size_t)(budget > 0 ? budget : 1) * 4;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     update_kernel<<<nseg, kUpdateThreads, smem, st>>>(scores, kept->Hkv, kept->S, seq_len, kept->top_idx,
-                                                     kept->top_count, kept->top_cap, budget, status);
+                                                     kept->top_count, kept->top_cap, hb, status);
     return cudaGetLastError();
 }
 

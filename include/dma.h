@@ -11,7 +11,9 @@
  *
  * Four calls make the forward hot path:
  *   dma_score_keys           s[b,h,j] = A_h * softplus(<V[b,j,h,:], W[h,:]>)
+ *                            (dma_score_keys_bias: also the bias s or exp(s))
  *   dma_select_topk          per-key top-set intervals + per-query-tile key lists
+ *                            (dma_select_topk_heads: a budget per KV head)
  *   dma_sparse_attn_prefill  masked softmax attention over the kept keys
  *   dma_sparse_attn_decode   the same for one new query row per sequence
  * plus page-granular decode over a paged KV cache (dma_score_keys_paged,
@@ -71,6 +73,11 @@ typedef enum { DMA_SEL_ROWWISE = 0, DMA_SEL_GLOBAL = 1 } dma_sel_mode_t;
  * newest key of each sequence into the top set of the previous row. */
 typedef enum { DMA_SEL_FULL = 0, DMA_SEL_UPDATE = 1 } dma_sel_op_t;
 
+/* What the logits get as their bias: LOG adds s = log delta (the default of
+ * every call taking `scores`); EXP adds the dynamic weight delta = exp(s)
+ * itself.  Either way the selection ranks s. */
+typedef enum { DMA_BIAS_LOG = 0, DMA_BIAS_EXP = 1 } dma_bias_form_t;
+
 /* Rows per query tile of the per-tile key lists. */
 #define DMA_Q_TILE 128
 
@@ -127,6 +134,19 @@ typedef struct {
 dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
                             int key_end, const float* W, const float* A, float* scores, dma_stream_t stream);
 
+/* dma_score_keys plus the bias array the attention calls take in place of the
+ * scores (DMA summary §五 writes the weight as delta = exp(tau(v Delta) * A)):
+ *   form    DMA_BIAS_LOG: bias = s (a copy of scores);
+ *           DMA_BIAS_EXP: bias = exp(s) in fp32 (+inf where s > about 88.7)
+ *   scores  device [B][Hkv][S] fp32   the ranking key, for dma_select_topk
+ *   bias    device [B][Hkv][S] fp32   non-NULL, not scores; for the attention
+ *           calls (prefill, decode, backward) as their `scores` argument
+ * Both written for key_begin <= j < key_end only.  exp is increasing, so
+ * ranking s keeps the sets that ranking delta would keep. */
+dma_status_t dma_score_keys_bias(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
+                                 int key_end, const float* W, const float* A, dma_bias_form_t form, float* scores,
+                                 float* bias, dma_stream_t stream);
+
 /* -------------------------------------------------------------- selection --
  * Fills the geometry of *kept for the given problem (pointers untouched) and
  * the workspace size dma_select_topk needs.  block is 1 (token units) or 64
@@ -155,6 +175,21 @@ dma_status_t dma_kept_layout(int B, int Hkv, int S, int w, int window, int block
 dma_status_t dma_select_topk(const float* scores, int B, int Hkv, int S, int w, int window, int block,
                              dma_sel_mode_t mode, dma_sel_op_t op, const int32_t* seq_len, dma_kept_t* kept,
                              void* ws, size_t ws_bytes, dma_stream_t stream);
+
+/* Per-KV-head budgets (Sparse Frontier summary, budget allocation: uniform vs
+ * adaptive across heads): dma_select_topk with KV head h of every sequence
+ * keeping w_head[h] keys (block units: floor(w_head[h] / 64) blocks) at every
+ * time step, selected exactly as a uniform budget of w_head[h] on that head.
+ *   w        the largest budget: kept's layout (dma_kept_layout with this w) is
+ *            sized for it, and the workspace is that of dma_select_topk
+ *   w_head   device [Hkv] int32, 0 <= w_head[h] <= w; read on the device, so an
+ *            entry outside the range is recorded as DMA_ERR_DEVICE_CHECK
+ *            (dma_get_device_status) and clamped into [0, w]
+ * Every other argument, and the result, as for dma_select_topk. */
+dma_status_t dma_select_topk_heads(const float* scores, int B, int Hkv, int S, int w, const int32_t* w_head,
+                                   int window, int block, dma_sel_mode_t mode, dma_sel_op_t op,
+                                   const int32_t* seq_len, dma_kept_t* kept, void* ws, size_t ws_bytes,
+                                   dma_stream_t stream);
 
 /* -------------------------------------------------------------- attention --
  * DMA summary §四/§五: masked positions are skipped outright; the kept ones get
@@ -257,6 +292,13 @@ dma_status_t dma_select_pages(const float* page_scores, int B, int Hkv, int max_
                               const int32_t* cache_len, int w, int32_t* top_idx, int32_t* top_count, int top_cap,
                               dma_stream_t stream);
 
+/* dma_select_pages with a budget per KV head: head h keeps floor(w_head[h] /
+ * page_size) pages.  w_head device [Hkv] int32 with 0 <= w_head[h] <= w (an entry
+ * outside is recorded as DMA_ERR_DEVICE_CHECK and clamped); top_cap as for w. */
+dma_status_t dma_select_pages_heads(const float* page_scores, int B, int Hkv, int max_pages, int page_size,
+                                    const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
+                                    int32_t* top_count, int top_cap, dma_stream_t stream);
+
 /* Decode over the kept pages and the window (bf16 only; H / Hkv <= 16): the same
  * result as dma_sparse_attn_decode over a contiguous cache holding the same rows.
  *   q, o, lse, scale, ws  as for dma_sparse_attn_decode (ws of
@@ -325,6 +367,15 @@ dma_status_t dma_sparse_attn_prefill_backward(const void* Q, const void* K, cons
 dma_status_t dma_score_keys_backward(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, const float* W,
                                      const float* A, const float* ds, float* dV, float* dW, float* dA, void* ws,
                                      size_t ws_bytes, dma_stream_t stream);
+
+/* dma_score_keys_backward for a bias of the given form: with DMA_BIAS_EXP, ds is
+ * the gradient of the added delta = exp(s), and the chain takes ds_j * delta_j
+ * as the gradient of s_j (delta recomputed from V, W, A).  Arguments otherwise
+ * as for dma_score_keys_backward. */
+dma_status_t dma_score_keys_backward_bias(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D,
+                                          const float* W, const float* A, dma_bias_form_t form, const float* ds,
+                                          float* dV, float* dW, float* dA, void* ws, size_t ws_bytes,
+                                          dma_stream_t stream);
 
 /* ------------------------------------------------------------------ misc -- */
 
