@@ -201,8 +201,9 @@ def config_keys(cfg, pairs, world=1):
 class Prefill:
     """Device buffers and the three calls of one prefill step for a workload."""
 
-    def __init__(self, dma, cfg, inp=None, block=None):
+    def __init__(self, dma, cfg, inp=None, block=None, form=0, w_head=None):
         self.dma, self.cfg = dma, cfg
+        self.form = form
         inp = wl.make_workload(cfg) if inp is None else inp
         self.inp = inp
         dev = torch.device("cuda")
@@ -212,6 +213,9 @@ class Prefill:
         self.block = cfg.block if block is None else block
         B, S, H, Hkv = cfg.B, cfg.S, cfg.H, cfg.Hkv
         self.scores = torch.empty((B, Hkv, S), dtype=torch.float32, device=dev)
+        # the logits' bias: the scores themselves, or delta = exp(s) in its own array
+        self.bias = self.scores if form == dma.BIAS_LOG else torch.empty_like(self.scores)
+        self.w_head = None if w_head is None else torch.tensor(w_head, dtype=torch.int32, device=dev)
         self.kept = dma.Kept(B, Hkv, S, cfg.w, cfg.window, self.block, dma.ROWWISE, device=dev)
         self.O = torch.empty_like(self.Q)
         self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
@@ -221,13 +225,19 @@ class Prefill:
         d = self.dma
         if ev:
             ev[0].record(stream)
-        d.dma_score_keys(self.V, self.W, self.A, self.scores, stream=stream)
+        if self.form == d.BIAS_LOG:
+            d.dma_score_keys(self.V, self.W, self.A, self.scores, stream=stream)
+        else:
+            d.dma_score_keys_bias(self.V, self.W, self.A, self.form, self.scores, self.bias, stream=stream)
         if ev:
             ev[1].record(stream)
-        d.dma_select_topk(self.scores, self.kept, d.FULL, stream=stream)
+        if self.w_head is None:
+            d.dma_select_topk(self.scores, self.kept, d.FULL, stream=stream)
+        else:
+            d.dma_select_topk_heads(self.scores, self.kept, self.w_head, d.FULL, stream=stream)
         if ev:
             ev[2].record(stream)
-        d.dma_sparse_attn_prefill(self.Q, self.K, self.V, self.scores, self.kept, self.O, self.lse, stream=stream)
+        d.dma_sparse_attn_prefill(self.Q, self.K, self.V, self.bias, self.kept, self.O, self.lse, stream=stream)
         if ev:
             ev[3].record(stream)
 
@@ -575,6 +585,8 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------ main ----
 
 PER_CONFIG = ["prefill_tiny_s256_fp32", "prefill_s4k_gqa_bf16", "prefill_s16k_bf16", "prefill_s64k_block64_bf16"]
+# a non-uniform allocation over the 8 KV heads of the 64K workload (at most its w = 4096)
+PER_HEAD_BUDGETS = [512, 1024, 2048, 4096, 4096, 2048, 1024, 512]
 
 
 def parity_vs_oracle(pf, ref):
@@ -713,6 +725,16 @@ def main():
                 del bw
             del p
             torch.cuda.empty_cache()
+        if cfg.name == PREFILL_WL:
+            # the two variants on the same 64K inputs: the exp-form bias, and a budget per KV head
+            for key, kw in (("prefill_s64k_bf16_exp_bias", dict(form=dma.BIAS_EXP)),
+                            ("prefill_s64k_bf16_per_head_budgets", dict(w_head=PER_HEAD_BUDGETS))):
+                p = Prefill(dma, cfg, inp=pf.inp, **kw)
+                per_config[key] = per_config_entry(p, p.timed(args.steps, args.warmup, world), peaks)
+                per_config[key].update({"bias": "exp(s)" if "form" in kw else "s",
+                                        "w_head": kw.get("w_head", [cfg.w] * cfg.Hkv)})
+                del p
+                torch.cuda.empty_cache()
     dec = None if args.no_decode else bench_decode(args, world)
     pdec = None if (args.no_decode or args.no_per_config) else bench_decode_paged(args, world)
     clk = clocks.stop()

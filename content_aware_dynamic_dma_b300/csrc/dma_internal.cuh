@@ -44,8 +44,12 @@ struct SelectPlan {
     int X;          // position block length of the 2-D count table
     int nX;         // ceil(n / X)
     int nlc;        // list chunks per segment (of the key and rank-order compactions)
+    int n_sg;       // super groups of query tiles per segment (1: the tile lists read the whole list)
+    int sg_tiles;   // query tiles per super group
+    int sg_cap;     // entries per super-group list
     // byte offsets into the workspace
     size_t off_key[2], off_val[2], off_hist, off_rank, off_tab, off_f0, off_bval, off_bexp, off_lcnt, off_krn;
+    size_t off_sgu, off_sge, off_sgn;
     size_t bytes;
 };
 

@@ -751,6 +751,81 @@ __global__ void __launch_bounds__(kListThreads) list_write_kernel(
     }
 }
 
+// ---------------------------------------------------- super-group lists ---
+
+// The entries of the rank-ordered ever-kept list that can reach a super group of
+// sg_tiles consecutive query tiles (the same tile-range test as the per-tile lists),
+// compacted in rank order.  Every per-tile list CTA of the super group then walks
+// this list instead of the whole one: on long sequences most ever-kept units live
+// for a short stretch of rows, so the super group's list is a fraction of the whole.
+// An entry reaching the rows [R0, R1] is in the top set of row R0 or enters it at a
+// later row, so a list holds at most k + (R1 - R0 + 1) entries (sg_cap).
+constexpr int kSgThreads = 1024;
+constexpr int kSgPer = 4;
+
+template <bool kBlocks>
+__global__ void __launch_bounds__(kSgThreads) sg_list_kernel(const int32_t* __restrict__ kr_u,
+                                                            const int32_t* __restrict__ kr_e,
+                                                            const int32_t* __restrict__ kr_n, int S, int n,
+                                                            int block, int window, int n_qt, int sg_tiles,
+                                                            int sg_cap, int32_t* __restrict__ sg_u,
+                                                            int32_t* __restrict__ sg_e, int32_t* __restrict__ sg_n,
+                                                            int* status)
+{
+    __shared__ int warp_buf[32];
+    const int seg = blockIdx.y, sg = blockIdx.x, n_sg = gridDim.x;
+    const int first = sg * sg_tiles, last = min(n_qt, first + sg_tiles) - 1;
+    const int bs = kBlocks ? block : 1;
+    const int32_t* ku = kr_u + (int64_t)seg * n;
+    const int32_t* ke = kr_e + (int64_t)seg * n;
+    int32_t* ou = sg_u + ((int64_t)seg * n_sg + sg) * sg_cap;
+    int32_t* oe = sg_e + ((int64_t)seg * n_sg + sg) * sg_cap;
+    const int m = min(max(kr_n[seg], 0), n);
+    int out = 0;
+    for (int base = 0; base < m; base += kSgThreads * kSgPer) {
+        int u[kSgPer], e[kSgPer];
+        unsigned keep = 0;
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kSgPer; ++i) {
+            const int q = base + (int)threadIdx.x * kSgPer + i;
+            u[i] = 0;
+            e[i] = 0;
+            if (q >= m) continue;
+            u[i] = ku[q];
+            e[i] = ke[q];
+            const int j0 = u[i] * bs;
+            if (u[i] < 0 || j0 >= S) {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+                continue;
+            }
+            if (e[i] <= 0) continue;
+            const int lo = top_lo(j0, block);
+            const int ta = max(lo / kQTile, window > 0 ? (j0 + window + kQTile - 1) / kQTile : j0 / kQTile);
+            const int tb = min(n_qt - 1, (e[i] - 1) / kQTile);
+            if (ta <= tb && ta <= last && tb >= first) {
+                keep |= 1u << i;
+                ++cnt;
+            }
+        }
+        int tot;
+        int o = out + block_exclusive_scan(cnt, warp_buf, &tot);
+#pragma unroll
+        for (int i = 0; i < kSgPer; ++i) {
+            if (!((keep >> i) & 1u)) continue;
+            if (o < sg_cap) {
+                ou[o] = u[i];
+                oe[o] = e[i];
+            } else {
+                set_status(status, DMA_ERR_DEVICE_CHECK);
+            }
+            ++o;
+        }
+        out += tot;
+    }
+    if (threadIdx.x == 0) sg_n[seg * n_sg + sg] = min(out, sg_cap);
+}
+
 // ----------------------------------------------------------- per-tile lists ---
 
 constexpr int kTileThreads = 256;
@@ -774,11 +849,16 @@ constexpr int kTilePartBytes = kTileGroup * kTilePartialCap * 4;
 // 32 entries at a time: once to count its keys per tile, once to write them at
 // its offsets; order within a warp comes from ballots (token units: one key per
 // entry) or warp scans (block units), across warps from one block-wide step.
+// kr_u, kr_e, kr_n: the ever-kept units in rank order with their expiry, per list (list_stride
+// entries apart) and their number; list l = seg * lists_per_seg + tile0 / tiles_per_list.
+// Token units fit four CTAs per SM (one wave on long sequences); block units take more
+// registers (the per-entry key counts): two CTAs per SM, which keeps them from spilling.
 template <bool kBlocks>
-__global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
-    const int32_t* __restrict__ kr_u, const int32_t* __restrict__ kr_e, const int32_t* __restrict__ kr_n, int S,
-    int n, int block, int window, int n_qt, int tile_stride, int bitmap_words, int32_t* __restrict__ tile_cnt,
-    int32_t* __restrict__ tile_idx, uint32_t* __restrict__ bitmap, int* status)
+__global__ void __launch_bounds__(kTileThreads, kBlocks ? 2 : 4) tile_list_kernel(
+    const int32_t* __restrict__ kr_u, const int32_t* __restrict__ kr_e, const int32_t* __restrict__ kr_n,
+    int list_stride, int lists_per_seg, int tiles_per_list, int S, int block, int window, int n_qt,
+    int tile_stride, int bitmap_words, int32_t* __restrict__ tile_cnt, int32_t* __restrict__ tile_idx,
+    uint32_t* __restrict__ bitmap, int* status)
 {
     // one byte per (tile, 64-key block), set by plain stores and packed into the bitmap at the
     // end; for long sequences (occ_smem false) the bits go straight to the bitmap in global
@@ -793,9 +873,10 @@ __global__ void __launch_bounds__(kTileThreads) tile_list_kernel(
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt = lanemask_lt();
     const int bs = kBlocks ? block : 1;
-    const int32_t* ku = kr_u + (int64_t)seg * n;
-    const int32_t* ke = kr_e + (int64_t)seg * n;
-    const int m = min(max(kr_n[seg], 0), n);
+    const int list = seg * lists_per_seg + tile0 / tiles_per_list;
+    const int32_t* ku = kr_u + (int64_t)list * list_stride;
+    const int32_t* ke = kr_e + (int64_t)list * list_stride;
+    const int m = min(max(kr_n[list], 0), list_stride);
     const int occ_len = bitmap_words * 32;
     const bool occ_smem = kTileGroup * occ_len <= kTileOccSmem;
     if (bitmap) {
@@ -1155,6 +1236,24 @@ SelectPlan make_select_plan(int B, int Hkv, int S, int w, int block)
     o = align_up(o + (size_t)pl.nseg * pl.nlc * 16, 256);
     pl.off_krn = o;
     o = align_up(o + (size_t)pl.nseg * 4, 256);
+    // super groups: at least 64 query tiles each (a multiple of the per-CTA group), at most 16
+    // of them per segment
+    const int n_qt = (S + kQTile - 1) / kQTile;
+    pl.sg_tiles = std::max(64, (n_qt + 15) / 16);
+    pl.sg_tiles = (pl.sg_tiles + kTileGroup - 1) / kTileGroup * kTileGroup;
+    pl.n_sg = (n_qt + pl.sg_tiles - 1) / pl.sg_tiles;
+    pl.sg_cap = (int)std::min<int64_t>(n, (int64_t)pl.k + (int64_t)pl.sg_tiles * kQTile + 1);
+    if (pl.n_sg > 1) {
+        const size_t nl = (size_t)pl.nseg * pl.n_sg;
+        pl.off_sgu = o;
+        o = align_up(o + nl * pl.sg_cap * 4, 256);
+        pl.off_sge = o;
+        o = align_up(o + nl * pl.sg_cap * 4, 256);
+        pl.off_sgn = o;
+        o = align_up(o + nl * 4, 256);
+    } else {
+        pl.off_sgu = pl.off_sge = pl.off_sgn = o;
+    }
     pl.bytes = o;
     return pl;
 }
@@ -1256,9 +1355,26 @@ cudaError_t launch_select_full(const float* scores, const SelectPlan& pl, const 
             if (smem > 48 * 1024 &&
                 (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
                 return e;
+            const int32_t *lu = kr_u, *le = kr_e, *ln = kr_n;
+            int stride = n, per_seg = 1, tiles = kept->n_qt;
+            if (pl.n_sg > 1) {
+                int32_t* sg_u = reinterpret_cast<int32_t*>(W + pl.off_sgu);
+                int32_t* sg_e = reinterpret_cast<int32_t*>(W + pl.off_sge);
+                int32_t* sg_n = reinterpret_cast<int32_t*>(W + pl.off_sgn);
+                auto sgk = block > 1 ? sg_list_kernel<true> : sg_list_kernel<false>;
+                sgk<<<dim3(pl.n_sg, nseg), kSgThreads, 0, st>>>(kr_u, kr_e, kr_n, S, n, block, kept->window,
+                                                                kept->n_qt, pl.sg_tiles, pl.sg_cap, sg_u, sg_e,
+                                                                sg_n, status);
+                lu = sg_u;
+                le = sg_e;
+                ln = sg_n;
+                stride = pl.sg_cap;
+                per_seg = pl.n_sg;
+                tiles = pl.sg_tiles;
+            }
             kern<<<dim3((kept->n_qt + kTileGroup - 1) / kTileGroup, nseg), kTileThreads, smem, st>>>(
-                kr_u, kr_e, kr_n, S, n, block, kept->window, kept->n_qt, kept->tile_stride, kept->bitmap_words,
-                kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
+                lu, le, ln, stride, per_seg, tiles, S, block, kept->window, kept->n_qt, kept->tile_stride,
+                kept->bitmap_words, kept->tile_cnt, kept->tile_idx, kept->bitmap, status);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
