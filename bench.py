@@ -50,9 +50,10 @@ PREFILL_WL = "prefill_s64k_bf16"
 DECODE_WL = "decode_b64_l32k_bf16"
 # launches of one FULL selection: 4 x (histogram, scatter) + count table + table prefix +
 # boundary + walk + list count + list write + tile lists; block units add the block maxima and
-# the expansion to keys
+# the expansion to keys; more than 64 query tiles (S > 8192) add the super-group lists
 LAUNCHES_SELECT_TOKEN = 15
 LAUNCHES_SELECT_BLOCK_EXTRA = 2
+LAUNCHES_SELECT_SUPER_GROUPS = 1
 LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merge
 
 # DRAM bytes (read + write) of one prefill attention launch on the 64K workload, from an ncu
@@ -219,7 +220,8 @@ class Prefill:
         self.kept = dma.Kept(B, Hkv, S, cfg.w, cfg.window, self.block, dma.ROWWISE, device=dev)
         self.O = torch.empty_like(self.Q)
         self.lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
-        self.launches = 1 + LAUNCHES_SELECT_TOKEN + (LAUNCHES_SELECT_BLOCK_EXTRA if self.block > 1 else 0) + 1
+        self.launches = (1 + LAUNCHES_SELECT_TOKEN + (LAUNCHES_SELECT_BLOCK_EXTRA if self.block > 1 else 0) +
+                         (LAUNCHES_SELECT_SUPER_GROUPS if S > 64 * 128 else 0) + 1)
 
     def calls(self, stream, ev=None):
         d = self.dma
