@@ -17,6 +17,8 @@ exactly -- bf16 is a subset of fp32 -- and every result is fp64):
 * ``score_backward(...)``       gradients through the score (dV, dW, dA)
 * ``backward(...)``             both, for a whole score -> select -> attend pass
 * ``kept_set(...)``             the kept key set of one row, from an expiry array
+* ``nsa_compress``, ``nsa_gates``, ``nsa_compressed_rows``, ``nsa_prefill``
+                                the NSA-style three-branch fusion (NSA post, §03)
 
 Method source: Dynamic Mask Attention summary (lsdiaocha.cn), §四 and §五.
 """
@@ -311,3 +313,87 @@ def top_set(expiry_seg: torch.Tensor, i: int, block: int = 1) -> set:
     """Top-set keys of row i (no window) for one (b, h) segment."""
     ex = expiry_seg.tolist()
     return {j for j in range(i + 1) if top_lo(j, block) <= i < ex[j]}
+
+
+# ------------------------------------------------------- NSA-style fusion --
+#
+# NSA post (news.news), §03: three branches run side by side -- attention over compressed
+# blocks (a coarse global view), over selected blocks (the important content) and over a
+# sliding window (local context) -- and a small gating network gives every token three
+# fusion weights.  Readings: a compressed block is the mean of the K (V) rows of a complete
+# 64-key block; the selected branch is the block-unit selection of this method (block
+# score = max of the key scores) with no window; no branch adds a bias; the gate of query
+# head h is sigmoid(<q, G[h, b]> + c[h, b]) for the branches b = compressed, selected,
+# window, and the output is the gate-weighted sum of the three branch outputs.
+
+NSA_BLOCK = 64
+
+
+def nsa_compress(K, V, block: int = NSA_BLOCK):
+    """Means of the complete blocks: (Kc, Vc) fp64 [B][S // block][Hkv][D]."""
+    B, S, Hkv, D = K.shape
+    nb = S // block
+    k = _f32(K).astype(np.float64)[:, :nb * block].reshape(B, nb, block, Hkv, D)
+    v = _f32(V).astype(np.float64)[:, :nb * block].reshape(B, nb, block, Hkv, D)
+    out_k = np.zeros((B, nb, Hkv, D), dtype=np.float64)
+    out_v = np.zeros((B, nb, Hkv, D), dtype=np.float64)
+    for t in range(block):           # the sum in key order, then one division
+        out_k += k[:, :, t]
+        out_v += v[:, :, t]
+    return torch.from_numpy(out_k / block), torch.from_numpy(out_v / block)
+
+
+def nsa_gates(Q, G, c):
+    """sigmoid(<Q[b, i, h], G[h, branch]> + c[h, branch]), fp64 [B][S][H][3]."""
+    q = _f32(Q).astype(np.float64)
+    g = _f32(G).astype(np.float64)
+    x = np.einsum("bihd,hgd->bihg", q, g) + _f32(c).astype(np.float64)[None, None]
+    return torch.from_numpy(1.0 / (1.0 + np.exp(-x)))
+
+
+def nsa_compressed_rows(Q, Kc, Vc, rows, block: int = NSA_BLOCK, scale: Optional[float] = None):
+    """Attention of the listed rows over the compressed blocks they see (block beta is seen by
+    row i iff its last key block * beta + block - 1 <= i); no bias.  Returns (O [B][n_rows][H][D],
+    lse [B][H][n_rows]) in fp64; a row that sees no block gets O = 0, lse = -inf."""
+    B, S, H, D = Q.shape
+    Hkv = Kc.shape[2]
+    G = H // Hkv
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    q = _f32(Q).astype(np.float64)
+    kc = Kc.to(torch.float64).numpy()
+    vc = Vc.to(torch.float64).numpy()
+    O = np.zeros((B, len(rows), H, D), dtype=np.float64)
+    lse = np.full((B, H, len(rows)), -np.inf, dtype=np.float64)
+    for r, i in enumerate(rows):
+        nv = (i + 1) // block    # blocks 0 .. nv-1 are complete by row i
+        if nv == 0:
+            continue
+        for b in range(B):
+            for h in range(H):
+                x = scale * (kc[b, :nv, h // G] @ q[b, i, h])
+                m = x.max()
+                p = np.exp(x - m)
+                l = p.sum()
+                O[b, r, h] = (p @ vc[b, :nv, h // G]) / l
+                lse[b, h, r] = m + math.log(l)
+    return torch.from_numpy(O), torch.from_numpy(lse)
+
+
+def nsa_prefill(Q, K, V, W, A, G, c, w, window: int, rows=None, scale: Optional[float] = None):
+    """The three branches and their gated sum for the listed rows.  Returns a dict with O (the
+    fused output, [B][n_rows][H][D]), the branch outputs o_cmp, o_slc, o_win and their lse, the
+    gates [B][n_rows][H][3], the scores and the selected branch's expiry; fp64."""
+    B, S, H, D = Q.shape
+    rows = list(range(S)) if rows is None else list(rows)
+    sc = score(V, W, A)
+    zero = torch.zeros_like(sc)
+    ex_slc = select(sc, w, NSA_BLOCK, ROWWISE)
+    o_slc, l_slc = attend_rows(Q, K, V, zero, ex_slc, rows, 0, NSA_BLOCK, scale)
+    never = torch.arange(S, dtype=torch.int32).expand(sc.shape).contiguous()
+    o_win, l_win = attend_rows(Q, K, V, zero, never, rows, window, 1, scale)
+    Kc, Vc = nsa_compress(K, V)
+    o_cmp, l_cmp = nsa_compressed_rows(Q, Kc, Vc, rows, NSA_BLOCK, scale)
+    g = nsa_gates(Q, G, c)[:, rows]
+    O = g[..., 0:1] * o_cmp + g[..., 1:2] * o_slc + g[..., 2:3] * o_win
+    return {"O": O, "o_cmp": o_cmp, "o_slc": o_slc, "o_win": o_win, "lse_cmp": l_cmp, "lse_slc": l_slc,
+            "lse_win": l_win, "gates": g, "scores": sc, "expiry": ex_slc}
