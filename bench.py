@@ -473,6 +473,85 @@ def bench_decode(args, world):
             "full_select_ms": full_ms, "full_select_keys": B * Hkv * L0}
 
 
+def bench_nsa(dma, pf, peaks, steps, warmup, world=1):
+    """The NSA-style three-branch step on the prefill workload's inputs: score, 64-key block
+    selection, block compression, the compressed, selected and sliding attentions, and the gated
+    sum.  TFLOP/s counts 4*D per kept pair over the three branches (exact counts: the compressed
+    blocks each row sees, the selection's intervals, the window band)."""
+    cfg = pf.cfg
+    B, S, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
+    G, c = wl.make_nsa_gates(H, D, cfg.seed)
+    G, c = G.cuda(), c.cuda()
+    st = dma.NsaPrefill(B, S, H, Hkv, D, cfg.w, cfg.window, dtype=pf.Q.dtype)
+    O = torch.empty_like(pf.Q)
+    stream = torch.cuda.current_stream()
+    names = ["score", "select", "compress", "attn_compressed", "attn_selected", "attn_window", "combine"]
+
+    def step(ev=None):
+        calls = [lambda: dma.dma_score_keys(pf.V, pf.W, pf.A, st.scores, stream=stream),
+                 lambda: dma.dma_select_topk(st.scores, st.kept_slc, dma.FULL, stream=stream),
+                 lambda: dma.dma_nsa_compress(pf.K, pf.V, st.Kc, st.Vc, stream=stream),
+                 lambda: dma.dma_sparse_attn_prefill(pf.Q, st.Kc, st.Vc, st.zero, st.kept_cmp, st.o_cmp, None,
+                                                     stream=stream),
+                 lambda: dma.dma_sparse_attn_prefill(pf.Q, pf.K, pf.V, st.zero, st.kept_slc, st.o_slc, None,
+                                                     stream=stream),
+                 lambda: dma.dma_sparse_attn_prefill(pf.Q, pf.K, pf.V, st.zero, st.kept_win, st.o_win, None,
+                                                     stream=stream),
+                 lambda: dma.dma_nsa_combine(pf.Q, st.o_cmp, st.o_slc, st.o_win, G, c, O, stream=stream)]
+        for i, call in enumerate(calls):
+            if ev:
+                ev[i].record(stream)
+            call()
+        if ev:
+            ev[len(calls)].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    assert dma.dma_get_device_status() == 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for s_ in range(steps):
+        step(ev[s_])
+    torch.cuda.synchronize()
+    barrier(world)
+    assert dma.dma_get_device_status() == 0
+    k_ms = {n: statistics.mean(ev[s_][i].elapsed_time(ev[s_][i + 1]) for s_ in range(steps))
+            for i, n in enumerate(names)}
+    total = max_over_ranks(statistics.mean(ev[s_][0].elapsed_time(ev[s_][-1]) for s_ in range(steps)), world)
+    G_ = H // Hkv
+    i = torch.arange(S, dtype=torch.int64)
+    p_cmp = int(((i + 1) // 64).sum()) * B * H
+    p_slc = kept_pairs(st.kept_slc.expiry, S, 0, 64, G_)
+    p_win = int(torch.clamp(i + 1, max=cfg.window).sum()) * B * H
+    pairs = p_cmp + p_slc + p_win
+    fl = 4.0 * D
+
+    def tf(p, ms):
+        return round(fl * p / (ms * 1e-3) / 1e12, 3)
+    comb_bytes = 5 * B * S * H * D * pf.Q.element_size()
+    ent = {"workload": cfg.name + "_nsa3", "B": B, "S": S, "H": H, "Hkv": Hkv, "D": D, "w": cfg.w,
+           "window": cfg.window, "block": 64, "kept_pairs": {"compressed": p_cmp, "selected": p_slc,
+                                                            "window": p_win},
+           "kernels_ms": {n: round(v, 4) for n, v in k_ms.items()}, "step_ms": round(total, 4),
+           "step_tflops": tf(pairs, total),
+           "attention_tflops": {"compressed": tf(p_cmp, k_ms["attn_compressed"]),
+                                "selected": tf(p_slc, k_ms["attn_selected"]),
+                                "window": tf(p_win, k_ms["attn_window"])},
+           "combine_gbs": round(comb_bytes / (k_ms["combine"] * 1e-3) / 1e9, 1),
+           "combine_frac_of_hbm": round(comb_bytes / (k_ms["combine"] * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+           "compress_gbs": round(2 * B * S * Hkv * D * pf.Q.element_size() / (k_ms["compress"] * 1e-3) / 1e9, 1),
+           "gates": "random-init G ~ N(0, 0.01), c ~ N(0, 1) (no trained gates)",
+           "fixed_patterns": "the compressed and window kept structures depend on S and the window only: "
+                             "built once, outside the timed steps"}
+    ent["attention_frac_of_bf16_peak"] = {k: round(v / peaks["bf16_tflops"], 4)
+                                          for k, v in ent["attention_tflops"].items()}
+    del st
+    torch.cuda.empty_cache()
+    return ent
+
+
 def bench_decode_paged(args, world, page_size=64):
     """The decode workload over a paged cache (pages of `page_size` tokens in random physical
     order): each step scores the new key and its page, selects the pages, and attends."""
@@ -737,6 +816,8 @@ def main():
                                         "w_head": kw.get("w_head", [cfg.w] * cfg.Hkv)})
                 del p
                 torch.cuda.empty_cache()
+            nsa = bench_nsa(dma, pf, peaks, args.steps, args.warmup, world)
+            per_config[nsa["workload"]] = nsa
     dec = None if args.no_decode else bench_decode(args, world)
     pdec = None if (args.no_decode or args.no_per_config) else bench_decode_paged(args, world)
     clk = clocks.stop()

@@ -18,10 +18,12 @@ The functions carry the C names:
   (``dma_score_keys_backward_bias``: for either form of the bias)
 * ``dma_score_keys_paged``, ``dma_select_pages`` (``dma_select_pages_heads``),
   ``dma_sparse_attn_decode_paged``: page-granular decode over a paged KV cache
+* ``dma_nsa_compress``, ``dma_nsa_kept_pattern``, ``dma_nsa_combine``: the NSA-style
+  three-branch fusion (compressed blocks, selected blocks, sliding window)
 
-plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and four
-compositions, ``prefill``, ``prefill_backward``, ``DecodeState`` and
-``PagedDecodeState``, for the common call sequences.
+plus ``Kept`` (the caller-owned kept-key arrays, allocated with torch) and the
+compositions ``prefill``, ``prefill_backward``, ``DecodeState``, ``PagedDecodeState``,
+``NsaPrefill`` and ``NsaDecode`` for the common call sequences.
 """
 from __future__ import annotations
 
@@ -50,6 +52,9 @@ FULL = 0
 UPDATE = 1
 BIAS_LOG = 0
 BIAS_EXP = 1
+NSA_COMPRESSED = 0
+NSA_WINDOW = 1
+NSA_BLOCK = 64
 Q_TILE = 128
 
 
@@ -74,7 +79,8 @@ EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_
             "dma_set_wait_limit_ns", "dma_set_fault_injection", "dma_version", "dma_backward_workspace_size",
             "dma_sparse_attn_prefill_backward", "dma_score_keys_backward", "dma_score_keys_paged",
             "dma_select_pages", "dma_sparse_attn_decode_paged", "dma_score_keys_bias", "dma_select_topk_heads",
-            "dma_select_pages_heads", "dma_score_keys_backward_bias")
+            "dma_select_pages_heads", "dma_score_keys_backward_bias", "dma_nsa_compress", "dma_nsa_kept_pattern",
+            "dma_nsa_combine")
 
 
 def _load_lib():
@@ -109,6 +115,9 @@ def _load_lib():
         "dma_select_topk_heads": [P, I, I, I, I, P, I, I, I, I, P, PK, P, Z, P],
         "dma_select_pages_heads": [P, I, I, I, I, P, I, P, P, P, I, P],
         "dma_score_keys_backward_bias": [P, I, I, I, I, I, P, P, I, P, P, P, P, P, Z, P],
+        "dma_nsa_compress": [P, P, I, I, I, I, I, I, I, P, P, P],
+        "dma_nsa_kept_pattern": [I, P, PK, P],
+        "dma_nsa_combine": [P, P, P, P, I, I, I, I, I, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -570,3 +579,128 @@ class PagedDecodeState:
         self.select(cache_len, stream)
         dma_sparse_attn_decode_paged(q, K_pages, V_pages, block_table, self.scores, self.top_idx, self.top_count,
                                      self.window, o, self.ws, lse, cache_len, scale, stream=stream)
+
+
+# ------------------------------------------------------- NSA-style fusion --
+
+def dma_nsa_compress(K: torch.Tensor, V: torch.Tensor, Kc: torch.Tensor, Vc: torch.Tensor, block_begin: int = 0,
+                     block_end: Optional[int] = None, stream=None) -> None:
+    """Means of the complete 64-key blocks, written at row 64 beta + 63 of Kc, Vc (shaped like K)."""
+    B, S, Hkv, D = K.shape
+    block_end = S // NSA_BLOCK if block_end is None else block_end
+    _check(_lib.dma_nsa_compress(_ptr(K), _ptr(V), _dtype(K), B, S, Hkv, D, block_begin, block_end, _ptr(Kc),
+                                 _ptr(Vc), _stream(stream)))
+
+
+def dma_nsa_kept_pattern(pattern: int, kept: Kept, seq_len: Optional[torch.Tensor] = None, stream=None) -> None:
+    _check(_lib.dma_nsa_kept_pattern(pattern, _ptr(seq_len), ctypes.byref(kept.t), _stream(stream)))
+
+
+def dma_nsa_combine(Q: torch.Tensor, O_cmp: torch.Tensor, O_slc: torch.Tensor, O_win: torch.Tensor,
+                    G: torch.Tensor, c: torch.Tensor, O: torch.Tensor, gates: Optional[torch.Tensor] = None,
+                    stream=None) -> None:
+    """Q and the outputs [B][S][H][D] ([B][H][D] for decode); G [H][3][D], c [H][3] fp32."""
+    if Q.dim() == 3:
+        B, H, D = Q.shape
+        S = 1
+    else:
+        B, S, H, D = Q.shape
+    _check(_lib.dma_nsa_combine(_ptr(Q), _ptr(O_cmp), _ptr(O_slc), _ptr(O_win), _dtype(Q), B, S, H, D, _ptr(G),
+                                _ptr(c), _ptr(O), _ptr(gates), _stream(stream)))
+
+
+class NsaPrefill:
+    """Buffers of the NSA-style three-branch prefill for one shape: the selected branch's
+    kept keys (64-key blocks, no window), the two fixed patterns (built once here), the
+    compressed K/V arrays, an all-zero bias and the three branch outputs."""
+
+    def __init__(self, B: int, S: int, H: int, Hkv: int, D: int, w: int, window: int, dtype=torch.bfloat16,
+                 device="cuda", stream=None):
+        self.B, self.S, self.H, self.Hkv, self.D, self.w, self.window = B, S, H, Hkv, D, w, window
+        f32 = dict(dtype=torch.float32, device=device)
+        self.scores = torch.empty((B, Hkv, S), **f32)
+        self.zero = torch.zeros((B, Hkv, S), **f32)
+        self.kept_slc = Kept(B, Hkv, S, w, 0, NSA_BLOCK, ROWWISE, device=device)
+        self.kept_cmp = Kept(B, Hkv, S, S // NSA_BLOCK, 0, 1, GLOBAL, device=device)
+        self.kept_win = Kept(B, Hkv, S, 0, window, 1, ROWWISE, device=device)
+        dma_nsa_kept_pattern(NSA_COMPRESSED, self.kept_cmp, stream=stream)
+        dma_nsa_kept_pattern(NSA_WINDOW, self.kept_win, stream=stream)
+        self.Kc = torch.zeros((B, S, Hkv, D), dtype=dtype, device=device)
+        self.Vc = torch.zeros((B, S, Hkv, D), dtype=dtype, device=device)
+        self.o_cmp, self.o_slc, self.o_win = (torch.empty((B, S, H, D), dtype=dtype, device=device)
+                                              for _ in range(3))
+
+    def run(self, Q, K, V, W, A, G, c, O, gates=None, scale: float = 0.0, stream=None):
+        """Score, select (64-key blocks), compress, the three attentions, the gated sum into O."""
+        dma_score_keys(V, W, A, self.scores, stream=stream)
+        dma_select_topk(self.scores, self.kept_slc, FULL, stream=stream)
+        dma_nsa_compress(K, V, self.Kc, self.Vc, stream=stream)
+        dma_sparse_attn_prefill(Q, self.Kc, self.Vc, self.zero, self.kept_cmp, self.o_cmp, None, scale, stream=stream)
+        dma_sparse_attn_prefill(Q, K, V, self.zero, self.kept_slc, self.o_slc, None, scale, stream=stream)
+        dma_sparse_attn_prefill(Q, K, V, self.zero, self.kept_win, self.o_win, None, scale, stream=stream)
+        dma_nsa_combine(Q, self.o_cmp, self.o_slc, self.o_win, G, c, O, gates, stream=stream)
+
+
+class NsaDecode:
+    """The NSA-style fusion for one new query row per sequence over caches [B][Lmax][Hkv][D]
+    (Lmax a multiple of 64).  The selected branch takes the decode row's 64-key blocks by page
+    selection over the contiguous cache viewed as 64-key pages (block table b * Lmax/64 + p),
+    the block-unit rule on the last row."""
+
+    def __init__(self, B: int, Lmax: int, H: int, Hkv: int, D: int, w: int, window: int, dtype=torch.bfloat16,
+                 device="cuda"):
+        if Lmax % NSA_BLOCK:
+            raise ValueError("Lmax must be a multiple of 64")
+        self.B, self.Lmax, self.H, self.Hkv, self.D, self.w, self.window = B, Lmax, H, Hkv, D, w, window
+        f32 = dict(dtype=torch.float32, device=device)
+        npg = Lmax // NSA_BLOCK
+        self.block_table = torch.arange(B * npg, dtype=torch.int32, device=device).view(B, npg)
+        self.scores = torch.zeros((B, Hkv, Lmax), **f32)
+        self.page_scores = torch.full((B, Hkv, npg), float("-inf"), **f32)
+        self.zero = torch.zeros((B, Hkv, Lmax), **f32)
+        self.kept_slc = Kept(B, Hkv, Lmax, w, 0, NSA_BLOCK, ROWWISE, device=device, tiles=False)
+        self.kept_cmp = Kept(B, Hkv, Lmax, npg, 0, 1, GLOBAL, device=device, tiles=False)
+        self.kept_win = Kept(B, Hkv, Lmax, 0, window, 1, ROWWISE, device=device, tiles=False)
+        dma_nsa_kept_pattern(NSA_WINDOW, self.kept_win)
+        self.Kc = torch.zeros((B, Lmax, Hkv, D), dtype=dtype, device=device)
+        self.Vc = torch.zeros((B, Lmax, Hkv, D), dtype=dtype, device=device)
+        cap = max(k.t.top_cap for k in (self.kept_slc, self.kept_cmp, self.kept_win))
+        self.ws = torch.empty((dma_decode_workspace_size(B, H, Hkv, D, cap, window),), dtype=torch.uint8,
+                              device=device)
+        self.o_cmp, self.o_slc, self.o_win = (torch.empty((B, H, D), dtype=dtype, device=device) for _ in range(3))
+
+    def _pages(self, X):
+        return X.view(self.B * (self.Lmax // NSA_BLOCK), NSA_BLOCK, self.Hkv, self.D)
+
+    def prepare(self, Kc, Vc, W, cache_len: torch.Tensor, length: int, A=None, stream=None):
+        """Scores, block scores and compressed blocks of the caches (keys below cache_len[b]; length
+        = the largest cache length), and the compressed branch's kept blocks."""
+        dma_score_keys_paged(self._pages(Vc), self.block_table, W, A, self.scores, self.page_scores, cache_len, 0,
+                             length, stream=stream)
+        dma_nsa_compress(Kc, Vc, self.Kc, self.Vc, 0, length // NSA_BLOCK, stream=stream)
+        dma_nsa_kept_pattern(NSA_COMPRESSED, self.kept_cmp, cache_len, stream=stream)
+
+    def step(self, q, Kc, Vc, W, cache_len: torch.Tensor, new_pos: int, G, c, o, A=None, scale: float = 0.0,
+             stream=None):
+        """One decode step for a token already written at ``new_pos`` (= cache_len - 1): its score
+        and block score; when it completes a block, that block's means and the compressed
+        branch's kept blocks; then the three branches and the gated sum into o."""
+        dma_score_keys_paged(self._pages(Vc), self.block_table, W, A, self.scores, self.page_scores, cache_len,
+                             new_pos, new_pos + 1, stream=stream)
+        if (new_pos + 1) % NSA_BLOCK == 0:
+            beta = new_pos // NSA_BLOCK
+            dma_nsa_compress(Kc, Vc, self.Kc, self.Vc, beta, beta + 1, stream=stream)
+            dma_nsa_kept_pattern(NSA_COMPRESSED, self.kept_cmp, cache_len, stream=stream)
+        self.attend(q, Kc, Vc, cache_len, G, c, o, scale, stream)
+
+    def attend(self, q, Kc, Vc, cache_len, G, c, o, scale: float = 0.0, stream=None):
+        """The block selection of the decode row cache_len[b] - 1, the three branches and their
+        gated sum."""
+        ks = self.kept_slc
+        dma_select_pages(self.page_scores, NSA_BLOCK, self.w, ks.top_idx, ks.top_count, cache_len, stream=stream)
+        dma_sparse_attn_decode(q, self.Kc, self.Vc, self.zero, self.kept_cmp, self.o_cmp, self.ws, None, cache_len,
+                               scale, stream=stream)
+        dma_sparse_attn_decode(q, Kc, Vc, self.zero, ks, self.o_slc, self.ws, None, cache_len, scale, stream=stream)
+        dma_sparse_attn_decode(q, Kc, Vc, self.zero, self.kept_win, self.o_win, self.ws, None, cache_len, scale,
+                               stream=stream)
+        dma_nsa_combine(q, self.o_cmp, self.o_slc, self.o_win, G, c, o, stream=stream)

@@ -613,4 +613,76 @@ dma_status_t dma_score_keys_backward_bias(const void* V, dma_dtype_t dt, int B, 
     return score_backward_impl(V, dt, B, S, Hkv, D, W, A, form, ds, dV, dW, dA, ws, ws_bytes, stream);
 }
 
+dma_status_t dma_nsa_compress(const void* K, const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D,
+                              int block_begin, int block_end, void* Kc, void* Vc, dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, Hkv, D);
+    if (s != DMA_OK) return s;
+    if (!K || !V || !Kc || !Vc) return fail(DMA_ERR_INVALID_ARG, "K, V, Kc and Vc must be non-NULL");
+    if (!aligned16(K) || !aligned16(V) || !aligned16(Kc) || !aligned16(Vc))
+        return fail(DMA_ERR_INVALID_ARG, "K, V, Kc, Vc must be 16-byte aligned");
+    if (Kc == K || Kc == V || Vc == K || Vc == V || Kc == Vc)
+        return fail(DMA_ERR_INVALID_ARG, "Kc and Vc must be arrays of their own");
+    if (block_begin < 0 || block_end < block_begin || block_end > S / 64)
+        return fail(DMA_ERR_INVALID_ARG, "block range [%d, %d) outside the %d complete blocks", block_begin, block_end,
+                    S / 64);
+    cudaError_t e = launch_nsa_compress(K, V, dt, B, S, Hkv, D, block_begin, block_end, Kc, Vc,
+                                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block compression launch");
+    return ok();
+}
+
+dma_status_t dma_nsa_kept_pattern(dma_nsa_pattern_t pattern, const int32_t* seq_len, dma_kept_t* kept,
+                                  dma_stream_t stream)
+{
+    if (!kept) return fail(DMA_ERR_INVALID_ARG, "kept is NULL");
+    dma_status_t s = check_kept_geometry(kept, kept->B, kept->Hkv, kept->S);
+    if (s != DMA_OK) return s;
+    if (pattern == DMA_NSA_COMPRESSED) {
+        if (kept->w != kept->S / 64 || kept->window != 0 || kept->block != 1 || kept->mode != DMA_SEL_GLOBAL)
+            return fail(DMA_ERR_INVALID_ARG,
+                        "the compressed pattern takes the layout (w = S / 64 = %d, window 0, block 1, GLOBAL); got "
+                        "(w=%d window=%d block=%d mode=%d)", kept->S / 64, kept->w, kept->window, kept->block,
+                        kept->mode);
+    } else if (pattern == DMA_NSA_WINDOW) {
+        if (kept->w != 0 || kept->block != 1)
+            return fail(DMA_ERR_INVALID_ARG, "the window pattern takes the layout (w = 0, block 1); got (w=%d block=%d)",
+                        kept->w, kept->block);
+    } else {
+        return fail(DMA_ERR_INVALID_ARG, "pattern=%d", (int)pattern);
+    }
+    if (!kept->expiry) return fail(DMA_ERR_INVALID_ARG, "kept->expiry is NULL");
+    if ((kept->idx == nullptr) != (kept->count == nullptr))
+        return fail(DMA_ERR_INVALID_ARG, "idx and count must both be set or both be NULL");
+    if ((kept->top_idx == nullptr) != (kept->top_count == nullptr))
+        return fail(DMA_ERR_INVALID_ARG, "top_idx and top_count must both be set or both be NULL");
+    if ((kept->tile_idx == nullptr) != (kept->tile_cnt == nullptr))
+        return fail(DMA_ERR_INVALID_ARG, "tile_idx and tile_cnt must both be set or both be NULL");
+    if (kept->bitmap && !kept->tile_idx) return fail(DMA_ERR_INVALID_ARG, "bitmap needs tile_idx/tile_cnt");
+    if (seq_len && !aligned4(seq_len)) return fail(DMA_ERR_INVALID_ARG, "seq_len must be 4-byte aligned");
+    int* status = nullptr;
+    if ((s = status_ptr(&status)) != DMA_OK) return s;
+    cudaError_t e = launch_nsa_pattern(pattern == DMA_NSA_COMPRESSED ? 1 : 0, kept, seq_len, status,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pattern launch");
+    return ok();
+}
+
+dma_status_t dma_nsa_combine(const void* Q, const void* O_cmp, const void* O_slc, const void* O_win, dma_dtype_t dt,
+                             int B, int S, int H, int D, const float* G, const float* c, void* O, float* gates,
+                             dma_stream_t stream)
+{
+    dma_status_t s = check_common(dt, B, S, H, D);
+    if (s != DMA_OK) return s;
+    if (!Q || !O_cmp || !O_slc || !O_win || !G || !c || !O)
+        return fail(DMA_ERR_INVALID_ARG, "Q, the three branch outputs, G, c and O must be non-NULL");
+    if (!aligned16(Q) || !aligned16(O_cmp) || !aligned16(O_slc) || !aligned16(O_win) || !aligned16(O) ||
+        !aligned4(G) || !aligned4(c) || (gates && !aligned4(gates)))
+        return fail(DMA_ERR_INVALID_ARG, "Q, the branch outputs and O must be 16-byte aligned; G, c, gates 4-byte");
+    cudaError_t e = launch_nsa_combine(Q, O_cmp, O_slc, O_win, dt, (int64_t)B * S * H, H, D, G, c, O, gates,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fusion launch");
+    return ok();
+}
+
 }  // extern "C"

@@ -64,6 +64,14 @@ dma_status_t set_error(dma_status_t s, const char* fmt, ...);
 cudaError_t launch_score(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin, int key_end,
                          const float* W, const float* A, float* scores, float* bias, int exp_form, cudaStream_t st);
 
+cudaError_t launch_nsa_compress(const void* K, const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D,
+                                int block_begin, int block_end, void* Kc, void* Vc, cudaStream_t st);
+cudaError_t launch_nsa_pattern(int compressed, const dma_kept_t* kept, const int32_t* seq_len, int* status,
+                               cudaStream_t st);
+cudaError_t launch_nsa_combine(const void* Q, const void* Oc, const void* Os, const void* Ow, dma_dtype_t dt,
+                               int64_t rows, int H, int D, const float* G, const float* c, void* O, float* gates,
+                               cudaStream_t st);
+
 cudaError_t launch_select_full(const float* scores, const SelectPlan& plan, const dma_kept_t* kept,
                                const int32_t* w_head, void* ws, int* status, cudaStream_t st);
 cudaError_t launch_select_update(const float* scores, const dma_kept_t* kept, const int32_t* seq_len,

@@ -119,13 +119,20 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(
             b_s[threadIdx.x] = j >= 0 ? sc[j] : 0.f;
         }
         __syncthreads();
-        // 8 threads per key row: K and V rows to fp32 shared memory
+        // 8 threads per key row: K and V rows to fp32 shared memory.  An empty slot (past the
+        // end of the list) gets zeros: its weight is 0, and 0 times stale shared memory (NaN
+        // bits left by an earlier kernel) would not be.
         {
             const int kr = threadIdx.x / 8, part = threadIdx.x % 8;
             const int j = j_s[kr];
             if (j >= 0) {
                 load_row_f32<T>(Kh + (int64_t)j * kv_row_stride, k_s[kr], D, part, 8);
                 load_row_f32<T>(Vh + (int64_t)j * kv_row_stride, v_s[kr], D, part, 8);
+            } else {
+                for (int d = part; d < D; d += 8) {
+                    k_s[kr][d] = 0.f;
+                    v_s[kr][d] = 0.f;
+                }
             }
         }
         __syncthreads();

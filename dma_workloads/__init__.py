@@ -143,6 +143,15 @@ def make_grad(shape, dtype: torch.dtype, seed: int) -> torch.Tensor:
     return _randn(g, tuple(shape)).to(dtype).contiguous()
 
 
+def make_nsa_gates(H: int, D: int, seed: int, g_std: float = 0.1):
+    """Seeded gate parameters of the three-branch fusion: G [H][3][D] ~ N(0, g_std^2) and
+    c [H][3] ~ N(0, 1), fp32 on the CPU (random-init weights: no trained gates exist here)."""
+    g = torch.Generator().manual_seed(seed * 7907 + 3)
+    G = _randn(g, (H, 3, D)) * g_std
+    c = _randn(g, (H, 3))
+    return G.contiguous(), c.contiguous()
+
+
 def paginate(Kc: torch.Tensor, page_size: int, seed: int, extra_pages: int = 0):
     """A paged copy of a contiguous cache Kc [B][L][Hkv][D]: pages [n_pages][page_size][Hkv][D]
     with the physical pages in seeded random order (plus `extra_pages` unused ones), and the

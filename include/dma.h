@@ -18,6 +18,8 @@
  *   dma_sparse_attn_decode   the same for one new query row per sequence
  * plus page-granular decode over a paged KV cache (dma_score_keys_paged,
  * dma_select_pages, dma_sparse_attn_decode_paged),
+ * the NSA-style three-branch fusion (dma_nsa_compress, dma_nsa_kept_pattern,
+ * dma_nsa_combine),
  * and two for the backward pass (training through the same mask):
  *   dma_sparse_attn_prefill_backward  dQ, dK, dV and ds over the kept pairs
  *   dma_score_keys_backward           ds -> dW, dA and the score's share of dV
@@ -376,6 +378,66 @@ dma_status_t dma_score_keys_backward_bias(const void* V, dma_dtype_t dt, int B, 
                                           const float* W, const float* A, dma_bias_form_t form, const float* ds,
                                           float* dV, float* dW, float* dA, void* ws, size_t ws_bytes,
                                           dma_stream_t stream);
+
+/* ------------------------------------------------------- NSA-style fusion --
+ * NSA post (news.news) §03: three branches side by side -- attention over
+ * compressed blocks (a coarse view of everything), over selected blocks (the
+ * important content) and over a sliding window (local context) -- mixed per
+ * token by three gates from a small network.  The post gives no formulas; this
+ * library reads them as:
+ *   compressed  block beta is the mean of the K (V) rows of the complete 64-key
+ *               block 64 beta .. 64 beta + 63, seen by rows i >= 64 beta + 63;
+ *   selected    this library's 64-key block selection (dma_select_topk, block
+ *               64) with no window;
+ *   sliding     the keys i - window + 1 .. i;
+ *   no branch adds a bias (pass an all-zero scores array to the attention calls);
+ *   gates       g_b = sigmoid(<q_i, G[h][b]> + c[h][b]) for b = compressed,
+ *               selected, sliding; O_i = sum_b g_b o_b,i.
+ * Each branch runs through dma_sparse_attn_prefill (or _decode) with its own
+ * kept structure; the compressed branch gathers from the arrays that
+ * dma_nsa_compress writes.
+ */
+
+/* Block means in the layout the attention calls gather from:
+ *   K, V    device [B][S][Hkv][D] (dtype dt)
+ *   Kc, Vc  device [B][S][Hkv][D] (dtype dt), arrays of their own: row
+ *           64 beta + 63 receives the mean of rows 64 beta .. 64 beta + 63 of
+ *           block beta (summed in key order in fp32, rounded once to dt); no
+ *           other row is written (nor read by the compressed pattern)
+ *   blocks  block_begin <= beta < block_end, 0 <= block_begin <= block_end <=
+ *           S / 64 (complete blocks only; decode compresses a block once, when
+ *           its last key arrives) */
+dma_status_t dma_nsa_compress(const void* K, const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D,
+                              int block_begin, int block_end, void* Kc, void* Vc, dma_stream_t stream);
+
+typedef enum { DMA_NSA_COMPRESSED = 0, DMA_NSA_WINDOW = 1 } dma_nsa_pattern_t;
+
+/* Writes the kept structure of a fixed pattern (it depends on S and the window
+ * only, so one structure serves every step and layer of that length):
+ *   COMPRESSED  key 64 beta + 63 of every complete block is kept from its own row
+ *               on, every other key never.  Layout: dma_kept_layout(B, Hkv, S,
+ *               w = S / 64, window = 0, block = 1, DMA_SEL_GLOBAL) -- the arrays
+ *               equal those of a global selection of the S / 64 best keys under
+ *               scores that rank exactly those keys first.
+ *   WINDOW      no key in any top set; the window alone.  Layout: dma_kept_layout(
+ *               B, Hkv, S, w = 0, window, block = 1, either mode).
+ *   seq_len     device [B] int32 or NULL (= S): top_idx/top_count become the
+ *               set of the decode row seq_len[b] - 1.
+ * Every array of *kept that is non-NULL is written (expiry is required). */
+dma_status_t dma_nsa_kept_pattern(dma_nsa_pattern_t pattern, const int32_t* seq_len, dma_kept_t* kept,
+                                  dma_stream_t stream);
+
+/* The gated sum of the three branch outputs:
+ *   Q                   device [B][S][H][D] (dtype dt)   the query rows (gate input)
+ *   O_cmp, O_slc, O_win device [B][S][H][D] (dtype dt)   branch outputs
+ *   G                   device [H][3][D] fp32            gate weights per query head
+ *   c                   device [H][3] fp32               gate offsets
+ *   O                   device [B][S][H][D] (dtype dt)   written (may alias a branch output)
+ *   gates               device [B][S][H][3] fp32 or NULL written when non-NULL
+ * Decode uses S = 1 (one row per sequence). */
+dma_status_t dma_nsa_combine(const void* Q, const void* O_cmp, const void* O_slc, const void* O_win, dma_dtype_t dt,
+                             int B, int S, int H, int D, const float* G, const float* c, void* O, float* gates,
+                             dma_stream_t stream);
 
 /* ------------------------------------------------------------------ misc -- */
 
