@@ -739,6 +739,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode only (a profiling aid: the line then carries no prefill metric)")
+    ap.add_argument("--nsa-only", action="store_true",
+                    help="the NSA-style three-branch step on the --workload inputs only (a profiling aid)")
     ap.add_argument("--decode-batch", type=int, default=wl.WORKLOADS[DECODE_WL].B,
                     help="sequences of the decode workload (smaller values serve profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -770,6 +772,13 @@ def main():
         return
     cfg = wl.WORKLOADS[args.workload]
     pf = Prefill(dma, cfg)
+    if args.nsa_only:
+        nsa = bench_nsa(dma, pf, peaks, args.steps, args.warmup, world)
+        if rank == 0:
+            print(json.dumps({"metric": "NSA-style three-branch step TFLOP/s", "value": nsa["step_tflops"],
+                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "nsa": nsa}), flush=True)
+        return
     clocks.start()
     r = pf.timed(args.steps, args.warmup, world)
     pairs = pf.pairs()
