@@ -401,7 +401,47 @@ def backward_entry(pf, r, peaks, steps):
 
 # ---------------------------------------------------------------- decode ----
 
-def bench_decode(args, world):
+def decode_parity(cfg, nq, st, o, lse, sample):
+    """The timed decode's last step (row L - 1 of every cache) against the oracle on the sampled
+    sequences, regenerated from their own seeds: the top sets compared exactly except near-tie
+    swaps (a KV head with one is left out of the output check), outputs with the tests' bound
+    (2e-2 on the arithmetic plus half a bf16 ulp for the output's rounding)."""
+    import numpy as np
+    import oracle
+    L, Hkv, H = cfg.S, cfg.Hkv, cfg.H
+    G = H // Hkv
+    h_inp = {k: (None if v is None else v.cpu())
+             for k, v in wl.make_workload(cfg, n_queries=nq, device="cuda", batches=sample).items()}
+    sc = oracle.score(h_inp["Vc"], h_inp["W"], None)
+    o_ref, lse_ref = oracle.decode(h_inp["q"][nq - 1], h_inp["Kc"], h_inp["Vc"], [L] * len(sample), sc, cfg.w,
+                                   cfg.window)
+    ex = oracle.select(sc, cfg.w)
+    keep = torch.ones((len(sample), H), dtype=torch.bool)
+    swaps = 0
+    for r, b in enumerate(sample):
+        for h in range(Hkv):
+            got = set(st.kept.top_idx[b, h, :int(st.kept.top_count[b, h])].tolist())
+            want = set(torch.nonzero(ex[r, h] >= L).flatten().tolist())
+            if got != want:
+                s32 = sc[r, h].numpy().astype(np.float32).astype(np.float64)
+                cut = min(s32[list(want)])
+                if any(abs(s32[j] - cut) > 1e-5 for j in got ^ want):
+                    return {"sequences": sample, "ok": False, "reason": "kept set differs beyond a near tie"}
+                keep[r, h * G:(h + 1) * G] = False
+                swaps += 1
+    g = o[sample].double().cpu()
+    _, e = torch.frexp(o_ref.abs())
+    half_ulp = torch.ldexp(torch.ones_like(o_ref), (e - 9).to(torch.int32))
+    err = (g - o_ref).abs().amax(dim=-1)
+    ex_half = ((g - o_ref).abs() - half_ulp).amax(dim=-1)
+    lse_err = (lse[sample].double().cpu() - lse_ref).abs()
+    return {"sequences": sample, "kv_heads_left_out_near_ties": swaps,
+            "max_abs_err": round(float(err[keep].max()), 5), "max_err_less_half_ulp": round(float(ex_half[keep].max()), 5),
+            "lse_max_abs_err": round(float(lse_err[keep].max()), 6),
+            "ok": bool(float(ex_half[keep].max()) <= 2e-2 and float(lse_err[keep].max()) <= 2e-2)}
+
+
+def bench_decode(args, world, check=False):
     import dataclasses
     import content_aware_dynamic_dma_b300 as dma
     cfg = wl.WORKLOADS[DECODE_WL]
@@ -467,10 +507,13 @@ def bench_decode(args, world):
     upd_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(n)]
     kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
     gbs = sum(kv_bytes) / (sum(dec_ms) * 1e-3) / 1e9
-    return {"workload": DECODE_WL if cfg.B == wl.WORKLOADS[DECODE_WL].B else "%s_b%d" % (DECODE_WL, cfg.B),
-            "gbs": gbs, "decode_ms": statistics.mean(dec_ms), "score_update_ms": statistics.mean(upd_ms),
-            "step_ms": step_ms, "selected_kv_bytes_per_step": statistics.mean(kv_bytes),
-            "full_select_ms": full_ms, "full_select_keys": B * Hkv * L0}
+    out = {"workload": DECODE_WL if cfg.B == wl.WORKLOADS[DECODE_WL].B else "%s_b%d" % (DECODE_WL, cfg.B),
+           "gbs": gbs, "decode_ms": statistics.mean(dec_ms), "score_update_ms": statistics.mean(upd_ms),
+           "step_ms": step_ms, "selected_kv_bytes_per_step": statistics.mean(kv_bytes),
+           "full_select_ms": full_ms, "full_select_keys": B * Hkv * L0}
+    if check:  # kept for the CPU-baseline leg, which checks this step against the oracle
+        out["_last_step"] = (cfg, nq, st, o, lse)
+    return out
 
 
 def bench_nsa(dma, pf, peaks, steps, warmup, world=1):
@@ -827,7 +870,7 @@ def main():
                 torch.cuda.empty_cache()
             nsa = bench_nsa(dma, pf, peaks, args.steps, args.warmup, world)
             per_config[nsa["workload"]] = nsa
-    dec = None if args.no_decode else bench_decode(args, world)
+    dec = None if args.no_decode else bench_decode(args, world, check=(rank == 0 and not args.no_cpu_baseline))
     pdec = None if (args.no_decode or args.no_per_config) else bench_decode_paged(args, world)
     clk = clocks.stop()
 
@@ -864,6 +907,7 @@ def main():
                           "score_and_update_ms": round(dec["score_update_ms"], 4),
                           "step_ms": round(dec["step_ms"], 4),
                           "selected_kv_bytes_per_step": dec["selected_kv_bytes_per_step"]}
+
         per_config[dec["workload"]] = {
             "update_select_and_score_ms": round(dec["score_update_ms"], 4),
             "full_select_ms": round(dec["full_select_ms"], 4), "full_select_keys": dec["full_select_keys"],
@@ -885,6 +929,19 @@ def main():
                                 "sample": desc, "seconds": round(secs, 2)}
         # the oracle rows of that sample, against the timed run's output
         line["parity"] = parity_vs_oracle(pf, ref)
+        if dec is not None and "_last_step" in dec:
+            # the oracle's decode of three sampled sequences, timed, against the timed decode's last step
+            dcfg, nq, dst, do, dlse = dec["_last_step"]
+            sample = sorted({0, dcfg.B // 2, dcfg.B - 1})
+            t0 = time.perf_counter()
+            dpar = decode_parity(dcfg, nq, dst, do, dlse, sample)
+            secs = time.perf_counter() - t0
+            line["cpu_baseline"]["decode"] = {
+                "sample": "%d of %d sequences: score, select and decode row of %d cached tokens" % (
+                    len(sample), dcfg.B, dcfg.S), "seconds": round(secs, 2),
+                "value": round(dec["selected_kv_bytes_per_step"] * len(sample) / dcfg.B / secs / 1e9, 6),
+                "unit": "GB/s of selected K/V (the oracle also scores and selects)"}
+            line["decode"]["parity"] = dpar
     print(json.dumps(line), flush=True)
 
 
