@@ -393,7 +393,7 @@ def nsa_prefill(Q, K, V, W, A, G, c, w, window: int, rows=None, scale: Optional[
     o_win, l_win = attend_rows(Q, K, V, zero, never, rows, window, 1, scale)
     Kc, Vc = nsa_compress(K, V)
     o_cmp, l_cmp = nsa_compressed_rows(Q, Kc, Vc, rows, NSA_BLOCK, scale)
-    g = nsa_gates(Q, G, c)[:, rows]
+    g = nsa_gates(Q[:, rows], G, c)
     O = g[..., 0:1] * o_cmp + g[..., 1:2] * o_slc + g[..., 2:3] * o_win
     return {"O": O, "o_cmp": o_cmp, "o_slc": o_slc, "o_win": o_win, "lse_cmp": l_cmp, "lse_slc": l_slc,
             "lse_win": l_win, "gates": g, "scores": sc, "expiry": ex_slc}

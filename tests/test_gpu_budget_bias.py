@@ -52,7 +52,8 @@ def check_bias(bias_gpu, sc_ref):
     assert bool((rel <= bound).all()), "bias error %.3g above its bound" % float((rel - bound).max())
 
 
-def run_case(dma, inp, w, window, block=1, mode=0, w_head=None, form="log", rows=None, check_tiles=True):
+def run_case(dma, inp, w, window, block=1, mode=0, w_head=None, form="log", rows=None, check_tiles=True,
+             tiles=None):
     """Score, select and attend on the GPU; compare with the oracle.  Returns the GPU arrays."""
     Q = inp["Q"]
     B, S, H, D = Q.shape
@@ -69,7 +70,7 @@ def run_case(dma, inp, w, window, block=1, mode=0, w_head=None, form="log", rows
     if form == "exp":
         check_bias(bias, sc)
     if check_tiles:
-        lists, bitmaps = parity.expected_tiles(ex, window, block)
+        lists, bitmaps = parity.expected_tiles(ex, window, block, tiles=tiles)
         tc, ti = kept.tile_cnt.cpu().numpy(), kept.tile_idx.cpu().numpy()
         bm = kept.bitmap.cpu().numpy().view(np.uint32)
         gs = dma_scores(dma, d)
@@ -122,6 +123,15 @@ def test_per_head_prefill_blocks_bf16(dma, mode):
     """64-key blocks: budgets of 10, 2, 1 (65 keys) and 0 (63 keys) blocks."""
     inp = wl.make_prefill(1, 2100, 8, 4, 128, torch.bfloat16, seed=3003 + mode, salient=True)
     run_case(dma, inp, 640, 64, block=64, mode=mode, w_head=[640, 128, 65, 63])
+
+
+def test_per_head_prefill_s64k_sampled_rows(dma):
+    """The 64K workload with budgets 512 .. 4096 over its eight KV heads (the bench's per-head
+    configuration): 128 sampled rows, six tiles' lists."""
+    cfg = wl.WORKLOADS["prefill_s64k_bf16"]
+    rows = wl.sample_rows(cfg.S, 128, cfg.seed, cfg.w)
+    run_case(dma, wl.make_workload(cfg), cfg.w, cfg.window, w_head=[512, 1024, 2048, 4096, 4096, 2048, 1024, 512],
+             rows=rows, tiles=[0, 31, 32, 33, 255, 511])
 
 
 @pytest.mark.parametrize("block,mode", [(1, 0), (1, 1), (64, 0), (64, 1)])

@@ -162,6 +162,15 @@ def test_nsa_prefill_s16k_bf16_sampled_rows(dma):
     run_nsa(dma, inp, G, c, cfg.w, cfg.window, rows=rows)
 
 
+def test_nsa_prefill_s64k_bf16_sampled_rows(dma):
+    """The bench's three-branch configuration: the 64K inputs, 64 sampled rows."""
+    cfg = wl.WORKLOADS["prefill_s64k_bf16"]
+    inp = wl.make_workload(cfg)
+    G, c = wl.make_nsa_gates(cfg.H, cfg.D, cfg.seed)
+    rows = wl.sample_rows(cfg.S, 64, cfg.seed, cfg.w)
+    run_nsa(dma, inp, G, c, cfg.w, cfg.window, rows=rows)
+
+
 def test_nsa_decode_steps_across_a_block_boundary(dma):
     """Steps from L = 1000 to 1030 (the block ending at key 1023 completes on the way); the
     final output against the oracle's last row over each sequence's prefix."""
