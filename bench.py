@@ -595,6 +595,57 @@ def bench_nsa(dma, pf, peaks, steps, warmup, world=1):
     return ent
 
 
+def bench_decode_nsa(args, world):
+    """The NSA-style three-branch decode on the decode workload: each step scores the new key
+    (and its 64-key block), compresses a block when the step completes one, selects the blocks
+    of the decode row, runs the compressed, selected and sliding decodes and the gated sum.
+    GB/s counts the K/V rows the three decodes read (compressed rows, selected blocks, window)."""
+    import dataclasses
+    import content_aware_dynamic_dma_b300 as dma
+    cfg = wl.WORKLOADS[DECODE_WL]
+    if args.decode_batch != cfg.B:
+        cfg = dataclasses.replace(cfg, B=args.decode_batch)
+    B, L, H, Hkv, D = cfg.B, cfg.S, cfg.H, cfg.Hkv, cfg.D
+    n = args.steps
+    nq = args.warmup + n
+    d = wl.make_workload(cfg, n_queries=nq, device="cuda")
+    G, c = wl.make_nsa_gates(H, D, cfg.seed)
+    G, c = G.cuda(), c.cuda()
+    st = dma.NsaDecode(B, L, H, Hkv, D, cfg.w, cfg.window)
+    L0 = L - nq
+    stream = torch.cuda.current_stream()
+    st.prepare(d["Kc"], d["Vc"], d["W"], torch.full((B,), L0, dtype=torch.int32, device="cuda"), L0,
+               stream=stream)
+    o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+    lens = [torch.full((B,), L0 + k + 1, dtype=torch.int32, device="cuda") for k in range(nq)]
+    for k in range(args.warmup):
+        st.step(d["q"][k], d["Kc"], d["Vc"], d["W"], lens[k], L0 + k, G, c, o, stream=stream)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    rows = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for s_ in range(n):
+        k = args.warmup + s_
+        pos = L0 + k
+        ev[s_][0].record(stream)
+        st.step(d["q"][k], d["Kc"], d["Vc"], d["W"], lens[k], pos, G, c, o, stream=stream)
+        ev[s_][1].record(stream)
+        Lk = pos + 1
+        # rows read: the compressed rows, the selected blocks' keys and the window (all heads)
+        rows.append(st.kept_slc.top_count.sum() + B * Hkv * (Lk // 64 + min(cfg.window, Lk)))
+    torch.cuda.synchronize()
+    barrier(world)
+    assert dma.dma_get_device_status() == 0
+    step_ms = [ev[s_][0].elapsed_time(ev[s_][1]) for s_ in range(n)]
+    kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
+    t = max_over_ranks(statistics.mean(step_ms), world)
+    return {"step_ms": round(t, 4), "kv_rows_bytes_per_step": statistics.mean(kv_bytes),
+            "gbs": round(statistics.mean(kv_bytes) / (t * 1e-3) / 1e9, 1),
+            "note": "whole step (score, block score, selection, three decodes, gated sum) against the K/V "
+                    "bytes the three decodes read"}
+
+
 def bench_decode_paged(args, world, page_size=64):
     """The decode workload over a paged cache (pages of `page_size` tokens in random physical
     order): each step scores the new key and its page, selects the pages, and attends."""
@@ -872,6 +923,7 @@ def main():
             per_config[nsa["workload"]] = nsa
     dec = None if args.no_decode else bench_decode(args, world, check=(rank == 0 and not args.no_cpu_baseline))
     pdec = None if (args.no_decode or args.no_per_config) else bench_decode_paged(args, world)
+    ndec = None if (args.no_decode or args.no_per_config) else bench_decode_nsa(args, world)
     clk = clocks.stop()
 
     if rank != 0:
@@ -920,6 +972,9 @@ def main():
             "decode_frac_of_hbm": round(pdec["gbs"] / peaks["hbm_gbs"], 4), "step_ms": round(pdec["step_ms"], 4),
             "selected_kv_bytes_per_step": pdec["selected_kv_bytes_per_step"],
             "layout": "K/V pages [n_pages][page_size][Hkv][D] in random physical order behind a block table"}
+    if ndec is not None:
+        ndec["frac_of_hbm"] = round(ndec["gbs"] / peaks["hbm_gbs"], 4)
+        per_config[DECODE_WL + "_nsa3"] = ndec
     if per_config:
         line["per_config"] = per_config
     if not args.no_cpu_baseline and world == 1:
