@@ -150,6 +150,29 @@ __global__ void nsa_pattern_tiles_kernel(int compressed, int S, int window, int 
     }
 }
 
+// kPer floats to consecutive elements, in one store of kPer * sizeof(T) bytes.
+template <typename T, int kPer>
+__device__ __forceinline__ void store_run(T* p, const float* v)
+{
+    if constexpr (sizeof(T) == 2) {
+        uint32_t u[kPer / 2];
+#pragma unroll
+        for (int e = 0; e < kPer / 2; ++e) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+            u[e] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        if constexpr (kPer == 4)
+            *reinterpret_cast<uint2*>(p) = make_uint2(u[0], u[1]);
+        else
+            *reinterpret_cast<uint32_t*>(p) = u[0];
+    } else {
+        if constexpr (kPer == 4)
+            *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        else
+            *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    }
+}
+
 // The gated sum: per (b, i, h) a warp forms the three gates from the query row, then the
 // weighted sum of the branch rows.  O may alias a branch output: each element is read
 // before the same thread writes it.
@@ -198,14 +221,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) nsa_combine_kernel(
         cb[br] = __ldg(c + h * 3 + br);
     }
     const int64_t step = n_warps / H;
-    for (int64_t bi = gw / H; bi < n_rows; bi += step) {
-        const int64_t r = bi * H + h;
-        const int64_t base = r * D + lane * kPer;
-        float q[kPer], oc[kPer], os[kPer], ow[kPer];
-        load_run<T, kPer>(Q + base, q);
-        load_run<T, kPer>(Oc + base, oc);
-        load_run<T, kPer>(Os + base, os);
-        load_run<T, kPer>(Ow + base, ow);
+    // two rows per iteration: the loads of both are in flight before either's arithmetic
+    auto finish = [&](int64_t r, const float* q, const float* oc, const float* os, const float* ow) {
         float g[3];
 #pragma unroll
         for (int br = 0; br < 3; ++br) {
@@ -216,15 +233,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32) nsa_combine_kernel(
             for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
             g[br] = 1.f / (1.f + expf(-(x + cb[br])));
         }
+        float v[kPer];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const float v = fmaf(g[0], oc[e], fmaf(g[1], os[e], g[2] * ow[e]));
-            if constexpr (sizeof(T) == 2)
-                O[base + e] = __float2bfloat16_rn(v);
-            else
-                O[base + e] = v;
-        }
+        for (int e = 0; e < kPer; ++e) v[e] = fmaf(g[0], oc[e], fmaf(g[1], os[e], g[2] * ow[e]));
+        store_run<T, kPer>(O + r * D + lane * kPer, v);
         if (gates && lane < 3) gates[r * 3 + lane] = lane == 0 ? g[0] : (lane == 1 ? g[1] : g[2]);
+    };
+    for (int64_t bi = gw / H; bi < n_rows; bi += 2 * step) {
+        const int64_t r0 = bi * H + h, r1 = (bi + step) * H + h;
+        const bool two = bi + step < n_rows;  // warp-uniform
+        float q0[kPer], oc0[kPer], os0[kPer], ow0[kPer], q1[kPer], oc1[kPer], os1[kPer], ow1[kPer];
+        const int64_t b0 = r0 * D + lane * kPer, b1 = r1 * D + lane * kPer;
+        load_run<T, kPer>(Q + b0, q0);
+        load_run<T, kPer>(Oc + b0, oc0);
+        load_run<T, kPer>(Os + b0, os0);
+        load_run<T, kPer>(Ow + b0, ow0);
+        if (two) {
+            load_run<T, kPer>(Q + b1, q1);
+            load_run<T, kPer>(Oc + b1, oc1);
+            load_run<T, kPer>(Os + b1, os1);
+            load_run<T, kPer>(Ow + b1, ow1);
+        }
+        finish(r0, q0, oc0, os0, ow0);
+        if (two) finish(r1, q1, oc1, os1, ow1);
     }
 }
 

@@ -96,7 +96,7 @@ def test_s16k_bf16_sampled_rows(dma):
 @pytest.mark.parametrize("block", [1, 64])
 def test_s64k_bf16_sampled_rows(dma, block):
     cfg = wl.WORKLOADS["prefill_s64k_bf16"]
-    rows = wl.sample_rows(cfg.S, 128, cfg.seed, cfg.w, block=64)
+    rows = wl.sample_rows(cfg.S, 256, cfg.seed, cfg.w, block=64)
     run_prefill_case(dma, wl.make_workload(cfg), cfg.w, cfg.window, block=block, rows=rows,
                      tiles=[0, 31, 32, 33, 255, 511])
 
