@@ -137,6 +137,48 @@ def test_prefill_and_decode_reject_before_launch(dma):
                                       need, None) == dma.DMA_ERR_UNSUPPORTED
 
 
+def test_variant_entries_reject_before_launch(dma):
+    """Per-head budgets, the bias form and the NSA-style calls check their arguments on the
+    host and return before any launch."""
+    lib = dma._lib
+    f = ctypes.c_void_p(0x10000)
+    k, ws = dma.dma_kept_layout(1, 2, 256, 64, 0, 1, dma.ROWWISE)
+    k.expiry = k.idx = k.count = 0x10000
+    # per-head selection without the budget array
+    assert lib.dma_select_topk_heads(f, 1, 2, 256, 64, None, 0, 1, 0, 0, None, ctypes.byref(k), f, ws,
+                                     None) == dma.DMA_ERR_INVALID_ARG
+    # misaligned budget array
+    assert lib.dma_select_topk_heads(f, 1, 2, 256, 64, ctypes.c_void_p(0x10002), 0, 1, 0, 0, None, ctypes.byref(k),
+                                     f, ws, None) == dma.DMA_ERR_INVALID_ARG
+    # the bias array must be its own array, and the form one of the two
+    assert lib.dma_score_keys_bias(f, 1, 1, 16, 2, 128, 0, 16, f, None, 1, f, f, None) == dma.DMA_ERR_INVALID_ARG
+    assert lib.dma_score_keys_bias(f, 1, 1, 16, 2, 128, 0, 16, f, None, 1, f, None, None) == dma.DMA_ERR_INVALID_ARG
+    assert lib.dma_score_keys_bias(f, 1, 1, 16, 2, 128, 0, 16, f, None, 7, f,
+                                   ctypes.c_void_p(0x20000), None) == dma.DMA_ERR_INVALID_ARG
+    assert lib.dma_score_keys_backward_bias(f, 1, 1, 16, 2, 128, f, None, 7, f, f, f, None, f, 1 << 20,
+                                            None) == dma.DMA_ERR_INVALID_ARG
+    # page selection per head without the budget array
+    assert lib.dma_select_pages_heads(f, 1, 2, 8, 64, None, 128, None, f, f, 128, None) == dma.DMA_ERR_INVALID_ARG
+    # NSA: a block range past the complete blocks, and Kc aliasing K
+    assert lib.dma_nsa_compress(f, ctypes.c_void_p(0x20000), 1, 1, 300, 2, 128, 0, 5, ctypes.c_void_p(0x30000),
+                                ctypes.c_void_p(0x40000), None) == dma.DMA_ERR_INVALID_ARG
+    assert lib.dma_nsa_compress(f, ctypes.c_void_p(0x20000), 1, 1, 300, 2, 128, 0, 4, f, ctypes.c_void_p(0x40000),
+                                None) == dma.DMA_ERR_INVALID_ARG
+    # NSA patterns: the compressed pattern takes the layout (S / 64, window 0, block 1, global)
+    kc, _ = dma.dma_kept_layout(1, 2, 256, 4, 0, 1, dma.GLOBAL)
+    kc.expiry = 0x10000
+    kr, _ = dma.dma_kept_layout(1, 2, 256, 4, 0, 1, dma.ROWWISE)
+    kr.expiry = 0x10000
+    assert lib.dma_nsa_kept_pattern(dma.NSA_COMPRESSED, None, ctypes.byref(kr), None) == dma.DMA_ERR_INVALID_ARG
+    kw, _ = dma.dma_kept_layout(1, 2, 256, 0, 32, 1, dma.ROWWISE)
+    assert lib.dma_nsa_kept_pattern(dma.NSA_WINDOW, None, ctypes.byref(kw), None) == dma.DMA_ERR_INVALID_ARG  # no expiry
+    assert lib.dma_nsa_kept_pattern(dma.NSA_WINDOW, None, ctypes.byref(kc), None) == dma.DMA_ERR_INVALID_ARG  # w != 0
+    assert lib.dma_nsa_kept_pattern(5, None, ctypes.byref(kc), None) == dma.DMA_ERR_INVALID_ARG
+    # the gated sum: D = 96 and NULL gate weights
+    assert lib.dma_nsa_combine(f, f, f, f, 1, 1, 16, 4, 96, f, f, f, None, None) == dma.DMA_ERR_UNSUPPORTED
+    assert lib.dma_nsa_combine(f, f, f, f, 1, 1, 16, 4, 128, None, f, f, None, None) == dma.DMA_ERR_INVALID_ARG
+
+
 def test_status_strings(dma):
     names = [dma._lib.dma_status_string(i).decode() for i in range(7)]
     assert names == ["DMA_OK", "DMA_ERR_INVALID_ARG", "DMA_ERR_UNSUPPORTED", "DMA_ERR_WORKSPACE", "DMA_ERR_CUDA",
