@@ -23,6 +23,7 @@
  * and two for the backward pass (training through the same mask):
  *   dma_sparse_attn_prefill_backward  dQ, dK, dV and ds over the kept pairs
  *   dma_score_keys_backward           ds -> dW, dA and the score's share of dV
+ *                                     (dma_score_keys_backward_bias: either bias form)
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and frees every buffer; the library never
@@ -40,7 +41,8 @@
  *     DMA_ERR_CUDA.  dma_last_error_message() gives a per-thread detail string.
  *     Conditions found on the device (a bounded wait that ran out, an internal
  *     capacity check) set a device status word read by dma_get_device_status.
- *   - Outputs alias no input.
+ *   - Outputs alias no input, except where a call says so (dma_nsa_combine's O may
+ *     be one of its branch outputs).
  */
 #ifndef DMA_H_
 #define DMA_H_
