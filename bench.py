@@ -621,29 +621,56 @@ def bench_decode_nsa(args, world):
     for k in range(args.warmup):
         st.step(d["q"][k], d["Kc"], d["Vc"], d["W"], lens[k], L0 + k, G, c, o, stream=stream)
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    # the step's calls, as NsaDecode.step makes them, with events between the parts
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
     rows = []
+    ks = st.kept_slc
     barrier(world)
     torch.cuda.synchronize()
     for s_ in range(n):
         k = args.warmup + s_
         pos = L0 + k
+        q = d["q"][k]
         ev[s_][0].record(stream)
-        st.step(d["q"][k], d["Kc"], d["Vc"], d["W"], lens[k], pos, G, c, o, stream=stream)
+        dma.dma_score_keys_paged(st._pages(d["Vc"]), st.block_table, d["W"], None, st.scores, st.page_scores,
+                                 lens[k], pos, pos + 1, stream=stream)
+        if (pos + 1) % 64 == 0:
+            dma.dma_nsa_compress(d["Kc"], d["Vc"], st.Kc, st.Vc, pos // 64, pos // 64 + 1, stream=stream)
+            dma.dma_nsa_kept_pattern(dma.NSA_COMPRESSED, st.kept_cmp, lens[k], stream=stream)
+        dma.dma_select_pages(st.page_scores, 64, cfg.w, ks.top_idx, ks.top_count, lens[k], stream=stream)
         ev[s_][1].record(stream)
+        dma.dma_sparse_attn_decode(q, st.Kc, st.Vc, st.zero, st.kept_cmp, st.o_cmp, st.ws, None, lens[k],
+                                   stream=stream)
+        ev[s_][2].record(stream)
+        dma.dma_sparse_attn_decode(q, d["Kc"], d["Vc"], st.zero, ks, st.o_slc, st.ws, None, lens[k], stream=stream)
+        dma.dma_sparse_attn_decode(q, d["Kc"], d["Vc"], st.zero, st.kept_win, st.o_win, st.ws, None, lens[k],
+                                   stream=stream)
+        ev[s_][3].record(stream)
+        dma.dma_nsa_combine(q, st.o_cmp, st.o_slc, st.o_win, G, c, o, stream=stream)
+        ev[s_][4].record(stream)
         Lk = pos + 1
         # rows read: the compressed rows, the selected blocks' keys and the window (all heads)
-        rows.append(st.kept_slc.top_count.sum() + B * Hkv * (Lk // 64 + min(cfg.window, Lk)))
+        rows.append((ks.top_count.sum(), B * Hkv * (Lk // 64), B * Hkv * min(cfg.window, Lk)))
     torch.cuda.synchronize()
     barrier(world)
     assert dma.dma_get_device_status() == 0
-    step_ms = [ev[s_][0].elapsed_time(ev[s_][1]) for s_ in range(n)]
-    kv_bytes = [int(r.item()) * 2 * D * 2 for r in rows]
-    t = max_over_ranks(statistics.mean(step_ms), world)
-    return {"step_ms": round(t, 4), "kv_rows_bytes_per_step": statistics.mean(kv_bytes),
-            "gbs": round(statistics.mean(kv_bytes) / (t * 1e-3) / 1e9, 1),
-            "note": "whole step (score, block score, selection, three decodes, gated sum) against the K/V "
-                    "bytes the three decodes read"}
+
+    def mean_ms(i0, i1):
+        return statistics.mean(ev[s_][i0].elapsed_time(ev[s_][i1]) for s_ in range(n))
+    t = max_over_ranks(mean_ms(0, 4), world)
+    row_b = 2 * D * 2
+    b_cmp = statistics.mean(int(r[1]) * row_b for r in rows)
+    b_sw = statistics.mean((int(r[0].item()) + int(r[2])) * row_b for r in rows)
+    dec_ms = mean_ms(1, 3)
+    return {"step_ms": round(t, 4), "kv_rows_bytes_per_step": b_cmp + b_sw,
+            "gbs": round((b_cmp + b_sw) / (t * 1e-3) / 1e9, 1),
+            "kernels_ms": {"score_block_score_select": round(mean_ms(0, 1), 4),
+                           "decode_compressed": round(mean_ms(1, 2), 4),
+                           "decode_selected_and_window": round(mean_ms(2, 3), 4),
+                           "gated_sum": round(mean_ms(3, 4), 4)},
+            "decode_gbs": round((b_cmp + b_sw) / (dec_ms * 1e-3) / 1e9, 1),
+            "note": "gbs: the whole step against the K/V bytes the three decodes read; decode_gbs: the three "
+                    "decode launches alone"}
 
 
 def bench_decode_paged(args, world, page_size=64):
@@ -974,6 +1001,7 @@ def main():
             "layout": "K/V pages [n_pages][page_size][Hkv][D] in random physical order behind a block table"}
     if ndec is not None:
         ndec["frac_of_hbm"] = round(ndec["gbs"] / peaks["hbm_gbs"], 4)
+        ndec["decode_frac_of_hbm"] = round(ndec["decode_gbs"] / peaks["hbm_gbs"], 4)
         per_config[DECODE_WL + "_nsa3"] = ndec
     if per_config:
         line["per_config"] = per_config
