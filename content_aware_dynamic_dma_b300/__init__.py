@@ -80,7 +80,7 @@ EXPORTED = ("dma_score_keys", "dma_kept_layout", "dma_select_topk", "dma_sparse_
             "dma_sparse_attn_prefill_backward", "dma_score_keys_backward", "dma_score_keys_paged",
             "dma_select_pages", "dma_sparse_attn_decode_paged", "dma_score_keys_bias", "dma_select_topk_heads",
             "dma_select_pages_heads", "dma_score_keys_backward_bias", "dma_nsa_compress", "dma_nsa_kept_pattern",
-            "dma_nsa_combine")
+            "dma_nsa_combine", "dma_score_keys_paged_bias")
 
 
 def _load_lib():
@@ -118,6 +118,7 @@ def _load_lib():
         "dma_nsa_compress": [P, P, I, I, I, I, I, I, I, P, P, P],
         "dma_nsa_kept_pattern": [I, P, PK, P],
         "dma_nsa_combine": [P, P, P, P, I, I, I, I, I, P, P, P, P, P],
+        "dma_score_keys_paged_bias": [P, I, I, P, I, I, I, P, I, I, I, I, P, P, I, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -369,6 +370,19 @@ def dma_score_keys_paged(V_pages: torch.Tensor, block_table: torch.Tensor, W: to
                                      _ptr(page_scores), _stream(stream)))
 
 
+def dma_score_keys_paged_bias(V_pages: torch.Tensor, block_table: torch.Tensor, W: torch.Tensor,
+                              A: Optional[torch.Tensor], form: int, scores: torch.Tensor, bias: torch.Tensor,
+                              page_scores: Optional[torch.Tensor] = None, cache_len: Optional[torch.Tensor] = None,
+                              key_begin: int = 0, key_end: Optional[int] = None, stream=None) -> None:
+    """dma_score_keys_paged plus the bias array (s, or exp(s) for BIAS_EXP) for the paged decode."""
+    n_pages, P, Hkv, D = V_pages.shape
+    B, max_pages = block_table.shape
+    key_end = max_pages * P if key_end is None else key_end
+    _check(_lib.dma_score_keys_paged_bias(_ptr(V_pages), _dtype(V_pages), n_pages, _ptr(block_table), B, max_pages,
+                                          P, _ptr(cache_len), Hkv, D, key_begin, key_end, _ptr(W), _ptr(A), form,
+                                          _ptr(scores), _ptr(page_scores), _ptr(bias), _stream(stream)))
+
+
 def dma_select_pages(page_scores: torch.Tensor, page_size: int, w: int, top_idx: torch.Tensor,
                      top_count: torch.Tensor, cache_len: Optional[torch.Tensor] = None, stream=None) -> None:
     B, Hkv, max_pages = page_scores.shape
@@ -543,11 +557,12 @@ class PagedDecodeState:
     the selected pages and the workspace."""
 
     def __init__(self, B: int, max_pages: int, page_size: int, H: int, Hkv: int, D: int, w: int, window: int,
-                 device="cuda", w_head: Optional[torch.Tensor] = None):
+                 device="cuda", w_head: Optional[torch.Tensor] = None, form: int = BIAS_LOG):
         self.B, self.max_pages, self.page_size, self.H, self.Hkv, self.D = B, max_pages, page_size, H, Hkv, D
-        self.w, self.window, self.w_head = w, window, w_head
+        self.w, self.window, self.w_head, self.form = w, window, w_head, form
         f32 = dict(dtype=torch.float32, device=device)
         self.scores = torch.zeros((B, Hkv, max_pages * page_size), **f32)
+        self.bias = self.scores if form == BIAS_LOG else torch.zeros_like(self.scores)
         self.page_scores = torch.full((B, Hkv, max_pages), float("-inf"), **f32)
         self.top_cap = max(1, (w // page_size) * page_size)
         self.top_idx = torch.zeros((B, Hkv, self.top_cap), dtype=torch.int32, device=device)
@@ -555,11 +570,18 @@ class PagedDecodeState:
         self.ws = torch.empty((dma_decode_workspace_size(B, H, Hkv, D, self.top_cap, window),), dtype=torch.uint8,
                               device=device)
 
+    def _score(self, V_pages, block_table, W, A, cache_len, key_begin, key_end, stream):
+        if self.form == BIAS_LOG:
+            dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, key_begin,
+                                 key_end, stream=stream)
+        else:
+            dma_score_keys_paged_bias(V_pages, block_table, W, A, self.form, self.scores, self.bias,
+                                      self.page_scores, cache_len, key_begin, key_end, stream=stream)
+
     def full_score(self, V_pages, block_table, W, A=None, cache_len=None, length: Optional[int] = None, stream=None):
         """Scores every key below ``length`` (all of the cache when None) and its page scores."""
         length = self.max_pages * self.page_size if length is None else length
-        dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, 0, length,
-                             stream=stream)
+        self._score(V_pages, block_table, W, A, cache_len, 0, length, stream)
 
     def select(self, cache_len=None, stream=None):
         """The kept pages of every sequence's decode row, from the page scores."""
@@ -574,10 +596,9 @@ class PagedDecodeState:
              scale: float = 0.0, stream=None):
         """One decode step for a token already written at logical position ``new_pos``
         (= cache_len - 1): score it, update its page's score, select the pages, attend."""
-        dma_score_keys_paged(V_pages, block_table, W, A, self.scores, self.page_scores, cache_len, new_pos,
-                             new_pos + 1, stream=stream)
+        self._score(V_pages, block_table, W, A, cache_len, new_pos, new_pos + 1, stream)
         self.select(cache_len, stream)
-        dma_sparse_attn_decode_paged(q, K_pages, V_pages, block_table, self.scores, self.top_idx, self.top_count,
+        dma_sparse_attn_decode_paged(q, K_pages, V_pages, block_table, self.bias, self.top_idx, self.top_count,
                                      self.window, o, self.ws, lse, cache_len, scale, stream=stream)
 
 

@@ -395,11 +395,15 @@ int page_shift(int page_size)
 }
 }  // namespace
 
-dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
-                                  int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
-                                  int key_begin, int key_end, const float* W, const float* A, float* scores,
-                                  float* page_scores, dma_stream_t stream)
+static dma_status_t score_paged_impl(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                     int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                     int key_begin, int key_end, const float* W, const float* A,
+                                     dma_bias_form_t form, float* scores, float* page_scores, float* bias,
+                                     dma_stream_t stream)
 {
+    if (form != DMA_BIAS_LOG && form != DMA_BIAS_EXP) return fail(DMA_ERR_INVALID_ARG, "form=%d", (int)form);
+    if (bias && (bias == scores || !aligned4(bias)))
+        return fail(DMA_ERR_INVALID_ARG, "bias must be a 4-byte aligned array of its own");
     const int ps = page_shift(page_size);
     if (ps < 0) return fail(DMA_ERR_UNSUPPORTED, "page_size=%d (supported: 16, 32, 64, 128)", page_size);
     if (max_pages < 1 || max_pages > 8192 || n_pages < 1)
@@ -418,10 +422,30 @@ dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pag
     int* status = nullptr;
     if ((s = status_ptr(&status)) != DMA_OK) return s;
     cudaError_t e = launch_score_paged(V_pages, dt, block_table, n_pages, B, max_pages, ps, Hkv, D, key_begin, key_end,
-                                       cache_len, W, A, scores, page_scores, status,
-                                       reinterpret_cast<cudaStream_t>(stream));
+                                       cache_len, W, A, scores, page_scores, bias, form == DMA_BIAS_EXP ? 1 : 0,
+                                       status, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged score launch");
     return ok();
+}
+
+dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                  int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                  int key_begin, int key_end, const float* W, const float* A, float* scores,
+                                  float* page_scores, dma_stream_t stream)
+{
+    return score_paged_impl(V_pages, dt, n_pages, block_table, B, max_pages, page_size, cache_len, Hkv, D, key_begin,
+                            key_end, W, A, DMA_BIAS_LOG, scores, page_scores, nullptr, stream);
+}
+
+dma_status_t dma_score_keys_paged_bias(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                       int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                       int key_begin, int key_end, const float* W, const float* A,
+                                       dma_bias_form_t form, float* scores, float* page_scores, float* bias,
+                                       dma_stream_t stream)
+{
+    if (!bias) return fail(DMA_ERR_INVALID_ARG, "bias is NULL (dma_score_keys_paged writes the scores alone)");
+    return score_paged_impl(V_pages, dt, n_pages, block_table, B, max_pages, page_size, cache_len, Hkv, D, key_begin,
+                            key_end, W, A, form, scores, page_scores, bias, stream);
 }
 
 static dma_status_t select_pages_impl(const float* page_scores, int B, int Hkv, int max_pages, int page_size,

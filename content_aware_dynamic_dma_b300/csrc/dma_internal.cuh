@@ -131,8 +131,8 @@ cudaError_t launch_score_bwd(const void* V, dma_dtype_t dt, int B, int S, int Hk
 // Paged decode cache (K/V pages [n_pages][1 << pshift][Hkv][D], block_table [B][max_pages]).
 cudaError_t launch_score_paged(const void* Vp, dma_dtype_t dt, const int32_t* bt, int n_pages, int B, int max_pages,
                                int pshift, int Hkv, int D, int key_begin, int key_end, const int32_t* cache_len,
-                               const float* W, const float* A, float* scores, float* page_scores, int* status,
-                               cudaStream_t st);
+                               const float* W, const float* A, float* scores, float* page_scores, float* bias,
+                               int exp_form, int* status, cudaStream_t st);
 cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int pshift,
                                 const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
                                 int32_t* top_count, int top_cap, int* status, cudaStream_t st);

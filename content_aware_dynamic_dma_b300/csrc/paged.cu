@@ -50,7 +50,9 @@ __global__ void __launch_bounds__(kPagedThreads) score_paged_kernel(const T* __r
                                                                     int key_end, const int32_t* __restrict__ cache_len,
                                                                     const float* __restrict__ W,
                                                                     const float* __restrict__ A,
-                                                                    float* __restrict__ scores, int* status)
+                                                                    float* __restrict__ scores,
+                                                                    float* __restrict__ bias, int exp_form,
+                                                                    int* status)
 {
     constexpr int kElem = 16 / sizeof(T);
     constexpr int kCPR = D / kElem;  // lanes per row: 8, 16 or 32
@@ -94,7 +96,11 @@ __global__ void __launch_bounds__(kPagedThreads) score_paged_kernel(const T* __r
         if (valid && part == 0) {
             // softplus(x) = max(x, 0) + log1p(exp(-|x|))
             const float sp = fmaxf(acc, 0.f) + log1pf(expf(-fabsf(acc)));
-            scores[((int64_t)b * Hkv + h) * Lmax + j] = (A ? A[h] : 1.f) * sp;
+            const float sv = (A ? A[h] : 1.f) * sp;
+            const int64_t o = ((int64_t)b * Hkv + h) * Lmax + j;
+            scores[o] = sv;
+            // the logits' bias, when asked for: s itself or (exp form) delta = exp(s)
+            if (bias) bias[o] = exp_form ? expf(sv) : sv;
         }
     }
 }
@@ -196,13 +202,14 @@ __global__ void __launch_bounds__(kSelectThreads) select_pages_kernel(const floa
 template <typename T, int D>
 cudaError_t score_paged_typed(const void* Vp, const int32_t* bt, int n_pages, int B, int max_pages, int pshift,
                               int Hkv, int key_begin, int key_end, const int32_t* cache_len, const float* W,
-                              const float* A, float* scores, float* page_scores, int* status, cudaStream_t st)
+                              const float* A, float* scores, float* page_scores, float* bias, int exp_form,
+                              int* status, cudaStream_t st)
 {
     const int nk = key_end - key_begin;
     dim3 grid((nk + kPagedWarps - 1) / kPagedWarps, B);
     score_paged_kernel<T, D><<<grid, kPagedThreads, 0, st>>>(static_cast<const T*>(Vp), bt, n_pages, max_pages,
                                                              pshift, Hkv, key_begin, key_end, cache_len, W, A, scores,
-                                                             status);
+                                                             bias, exp_form, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !page_scores) return e;
     const int p_begin = key_begin >> pshift, n_p = ((key_end - 1) >> pshift) - p_begin + 1;
@@ -216,19 +223,21 @@ cudaError_t score_paged_typed(const void* Vp, const int32_t* bt, int n_pages, in
 
 cudaError_t launch_score_paged(const void* Vp, dma_dtype_t dt, const int32_t* bt, int n_pages, int B, int max_pages,
                                int pshift, int Hkv, int D, int key_begin, int key_end, const int32_t* cache_len,
-                               const float* W, const float* A, float* scores, float* page_scores, int* status,
-                               cudaStream_t st)
+                               const float* W, const float* A, float* scores, float* page_scores, float* bias,
+                               int exp_form, int* status, cudaStream_t st)
 {
     if (key_end <= key_begin) return cudaSuccess;
     if (dt == DMA_BF16)
         return D == 128 ? score_paged_typed<__nv_bfloat16, 128>(Vp, bt, n_pages, B, max_pages, pshift, Hkv, key_begin,
-                                                                key_end, cache_len, W, A, scores, page_scores, status, st)
+                                                                key_end, cache_len, W, A, scores, page_scores, bias,
+                                                                exp_form, status, st)
                         : score_paged_typed<__nv_bfloat16, 64>(Vp, bt, n_pages, B, max_pages, pshift, Hkv, key_begin,
-                                                               key_end, cache_len, W, A, scores, page_scores, status, st);
+                                                               key_end, cache_len, W, A, scores, page_scores, bias,
+                                                               exp_form, status, st);
     return D == 128 ? score_paged_typed<float, 128>(Vp, bt, n_pages, B, max_pages, pshift, Hkv, key_begin, key_end,
-                                                    cache_len, W, A, scores, page_scores, status, st)
+                                                    cache_len, W, A, scores, page_scores, bias, exp_form, status, st)
                     : score_paged_typed<float, 64>(Vp, bt, n_pages, B, max_pages, pshift, Hkv, key_begin, key_end,
-                                                   cache_len, W, A, scores, page_scores, status, st);
+                                                   cache_len, W, A, scores, page_scores, bias, exp_form, status, st);
 }
 
 cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int max_pages, int pshift,

@@ -287,6 +287,17 @@ dma_status_t dma_score_keys_paged(const void* V_pages, dma_dtype_t dt, int n_pag
                                   int key_begin, int key_end, const float* W, const float* A, float* scores,
                                   float* page_scores, dma_stream_t stream);
 
+/* dma_score_keys_paged plus the bias array the paged decode takes as its scores
+ * (the exp form of dma_score_keys_bias for a paged cache): bias [B][Hkv][max_pages *
+ * page_size] fp32, non-NULL and not scores, receives s (DMA_BIAS_LOG) or exp(s)
+ * (DMA_BIAS_EXP) for the keys scored; the page scores stay the maxima of s, so
+ * the page selection is unchanged. */
+dma_status_t dma_score_keys_paged_bias(const void* V_pages, dma_dtype_t dt, int n_pages, const int32_t* block_table,
+                                       int B, int max_pages, int page_size, const int32_t* cache_len, int Hkv, int D,
+                                       int key_begin, int key_end, const float* W, const float* A,
+                                       dma_bias_form_t form, float* scores, float* page_scores, float* bias,
+                                       dma_stream_t stream);
+
 /* The kept pages of every sequence's decode row, written as their keys:
  *   top_idx    device [B][Hkv][top_cap] int32: the keys of the kept pages, ascending
  *   top_count  device [B][Hkv] int32: their number

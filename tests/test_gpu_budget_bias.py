@@ -373,3 +373,47 @@ def test_exp_decode_update(dma):
     o_ref, lse_ref = oracle.decode(inp["q"][n - 1], inp["Kc"], inp["Vc"], [L] * B, sc, w, window, bias=delta)
     assert float(((o.double().cpu() - o_ref).abs() - parity.out_tol(o_ref, torch.bfloat16)).max()) <= 0
     assert float((lse.double().cpu() - lse_ref).abs().max()) <= 2e-2
+
+
+def test_exp_paged_decode(dma):
+    """The exp form over a paged cache: the bias array beside the scores, the page selection on
+    the scores, the decode against the oracle's decode given delta as the bias (block = page)."""
+    B, L, H, Hkv, D, w, window, P = 3, 1000, 8, 2, 128, 256, 32, 64
+    dd = wl.make_decode(B, L, H, Hkv, D, torch.bfloat16, seed=3015, salient=False, device="cuda")
+    lens = [1000, 700, 130]
+    Kp, bt = wl.paginate(dd["Kc"], P, 7, 2)
+    Vp, _ = wl.paginate(dd["Vc"], P, 7, 2)
+    st = dma.PagedDecodeState(B, bt.shape[1], P, H, Hkv, D, w, window, form=dma.BIAS_EXP)
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    st.full_score(Vp, bt, dd["W"], cache_len=cl)
+    st.select(cl)
+    o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+    dma.dma_sparse_attn_decode_paged(dd["q"][0], Kp, Vp, bt, st.bias, st.top_idx, st.top_count, window, o, st.ws,
+                                     None, cl)
+    ref = torch.zeros((B, Hkv, L), dtype=torch.float32, device="cuda")
+    dma.dma_score_keys(dd["Vc"], dd["W"], None, ref)
+    torch.cuda.synchronize()
+    assert dma.dma_get_device_status() == 0
+    for b in range(B):
+        assert torch.equal(st.scores[b, :, :lens[b]], ref[b, :, :lens[b]])
+    h = {k: (None if v is None else v.cpu()) for k, v in dd.items()}
+    sc = oracle.score(h["Vc"], h["W"], None)
+    for b in range(B):
+        check_bias(st.bias[b:b + 1, :, :lens[b]], sc[b:b + 1, :, :lens[b]])
+    want = oracle.select_pages(sc, lens, P, w)
+    keep = torch.ones((B, H), dtype=torch.bool)
+    for b in range(B):
+        for hh in range(Hkv):
+            keys = st.top_idx[b, hh, :int(st.top_count[b, hh])].cpu().tolist()
+            pages = sorted(set(j // P for j in keys))
+            if pages != want[(b, hh)]:
+                # only a near tie may swap a page: its fp32 page score within 1e-5 of the cutoff
+                pm = [float(np.float32(sc[b, hh, p * P:(p + 1) * P].max())) for p in range(lens[b] // P)]
+                cut = sorted(pm, reverse=True)[len(want[(b, hh)]) - 1]
+                for p in set(pages) ^ set(want[(b, hh)]):
+                    assert abs(pm[p] - cut) <= parity.TIE_TOL, (b, hh, p)
+                keep[b, hh * (H // Hkv):(hh + 1) * (H // Hkv)] = False
+    delta = oracle.score(h["Vc"], h["W"], None, form="exp")
+    o_ref, _ = oracle.decode(h["q"][0], h["Kc"], h["Vc"], lens, sc, w, window, block=P, bias=delta)
+    err = ((o.double().cpu() - o_ref).abs() - parity.out_tol(o_ref, torch.bfloat16)).amax(dim=-1)
+    assert float(torch.where(keep, err, torch.full_like(err, -1.0)).max()) <= 0
