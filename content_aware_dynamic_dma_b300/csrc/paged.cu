@@ -176,7 +176,31 @@ __global__ void __launch_bounds__(kSelectThreads) select_pages_kernel(const floa
     const int k = min(wb >> pshift, n_c);
     const float* ps = page_scores + (int64_t)seg * max_pages;
     const int P = 1 << pshift;
-    if (k < n_c) {
+    if (k < n_c && n_c <= kSelectThreads) {
+        // one thread per complete page: its rank is the number of pages that beat it (the same
+        // (score rank, page index) order), and it is kept iff that is below k; the kept pages go
+        // out in page order through a block-wide prefix of the kept flags
+        __shared__ int warp_kept[kSelectThreads / 32];
+        for (int i = threadIdx.x; i < n_c; i += blockDim.x)
+            keys[i] = ((unsigned long long)rank_key(ps[i]) << 32) | (unsigned)i;
+        __syncthreads();
+        bool kept = false;
+        if ((int)threadIdx.x < n_c) {
+            const unsigned long long mine = keys[threadIdx.x];
+            int rank = 0;
+#pragma unroll 8
+            for (int q = 0; q < n_c; ++q) rank += keys[q] < mine ? 1 : 0;
+            kept = rank < k;
+        }
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        const unsigned bal = __ballot_sync(0xffffffffu, kept);
+        if (lane == 0) warp_kept[wid] = __popc(bal);
+        __syncthreads();  // every rank is counted before keys[] is reused below
+        int before = __popc(bal & ((1u << lane) - 1u));
+        for (int w2 = 0; w2 < wid; ++w2) before += warp_kept[w2];
+        if (kept) keys[before] = (unsigned)threadIdx.x;
+        __syncthreads();
+    } else if (k < n_c) {
         int n = 1;
         while (n < n_c) n <<= 1;
         // best first: (score rank, page index) ascending
