@@ -60,8 +60,8 @@ LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merg
 # capture of that launch itself (metrics dram__bytes_read.sum and dram__bytes_write.sum only,
 # one pass).  Valid only for the kernel source it was taken on: reported as null once that
 # source changes.
-PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 887806976 + 510288384,
-                   "source_sha256": "1545061eed7c18f4c0b171052e4ef87dca1d6db5d613953ead5ce858ae3dbe52"}
+PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 897375232 + 510041600,
+                   "source_sha256": "b0b1ae010a817dab280d094b1868c71f875cf5fd29256395239b1b71a46f3cae"}
 
 
 def load_peaks():
