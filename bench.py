@@ -61,7 +61,7 @@ LAUNCHES_PER_DECODE_STEP = 4  # score (new key) + update + decode partial + merg
 # one pass).  Valid only for the kernel source it was taken on: reported as null once that
 # source changes.
 PREFILL_TRAFFIC = {"workload": "prefill_s64k_bf16", "bytes": 897375232 + 510041600,
-                   "source_sha256": "b0b1ae010a817dab280d094b1868c71f875cf5fd29256395239b1b71a46f3cae"}
+                   "source_sha256": "a07b9592472bb1a84f4ba0787d8b8ba56e035a12100a5483ac65c8e83da5c849"}
 
 
 def load_peaks():

@@ -24,7 +24,7 @@
 //                    of a pass
 //   warp 12          MMA issue (one thread): S = Q K^T (both operands in shared
 //                    memory), O += P V (P from tensor memory, V in shared memory)
-//   warp 13          key metadata: runs up to four blocks ahead, filling a ring
+//   warp 13          key metadata: runs up to eight blocks ahead, filling a ring
 //                    with each block's key indices, bias (score, log2 units),
 //                    keep intervals and an "every row keeps every key" flag
 //   warps 14-15      copies: Q tiles and the K and V rows of each block,
