@@ -198,6 +198,7 @@ static dma_status_t score_impl(const void* V, dma_dtype_t dt, int B, int S, int 
     if (form != DMA_BIAS_LOG && form != DMA_BIAS_EXP) return fail(DMA_ERR_INVALID_ARG, "form=%d", (int)form);
     if (key_begin < 0 || key_end < key_begin || key_end > S)
         return fail(DMA_ERR_INVALID_ARG, "key range [%d, %d) outside [0, %d]", key_begin, key_end, S);
+    if (Hkv > 128) return fail(DMA_ERR_UNSUPPORTED, "scoring takes up to 128 KV heads (Hkv=%d)", Hkv);
     cudaError_t e = launch_score(V, dt, B, S, Hkv, D, key_begin, key_end, W, A, scores, bias,
                                  form == DMA_BIAS_EXP ? 1 : 0, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");

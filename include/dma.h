@@ -133,7 +133,8 @@ typedef struct {
  *   W       device [Hkv][D] fp32               per-KV-head sampling weights
  *   A       device [Hkv] fp32 or NULL (= 1)    per-KV-head gate
  *   scores  device [B][Hkv][S] fp32            written for key_begin <= j < key_end only
- * 0 <= key_begin <= key_end <= S.  key_begin == key_end is a no-op.
+ * 0 <= key_begin <= key_end <= S.  key_begin == key_end is a no-op.  Hkv <= 128
+ * (DMA_ERR_UNSUPPORTED otherwise, before any launch).
  */
 dma_status_t dma_score_keys(const void* V, dma_dtype_t dt, int B, int S, int Hkv, int D, int key_begin,
                             int key_end, const float* W, const float* A, float* scores, dma_stream_t stream);

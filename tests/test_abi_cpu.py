@@ -85,6 +85,9 @@ def test_score_rejects_before_launch(dma):
     # bad dtype
     assert lib.dma_score_keys(fake, 5, 1, 16, 2, 128, 0, 16, fake, None, fake, None) == dma.DMA_ERR_INVALID_ARG
     assert "key range" not in lib.dma_last_error_message().decode()
+    # more KV heads than one scoring CTA's rows
+    assert lib.dma_score_keys(fake, 1, 1, 16, 129, 64, 0, 16, fake, None, fake, None) == dma.DMA_ERR_UNSUPPORTED
+    assert "128 KV heads" in lib.dma_last_error_message().decode()
 
 
 def test_select_rejects_before_launch(dma):
