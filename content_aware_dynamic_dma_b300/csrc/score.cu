@@ -118,8 +118,9 @@ template <typename T, int D>
 cudaError_t launch_typed(const void* V, int B, int S, int Hkv, int key_begin, int key_end, const float* W,
                          const float* A, float* scores, float* bias, int exp_form, cudaStream_t st)
 {
-    // keys per CTA: as many as fill its rows (at least one key: a wider row count than a CTA's
-    // rows leaves the rest of the heads' rows out, which the argument checks rule out)
+    // keys per CTA: as many as fill its rows (the entry point accepts at most 128 KV heads, no
+    // more than the rows of any instantiation, so every CTA covers at least one whole key)
+    static_assert(score_rows_per_cta<T, D>() >= 128, "a CTA covers the rows of one key of 128 KV heads");
     const int TJ = std::max(1, score_rows_per_cta<T, D>() / Hkv);
     dim3 grid((key_end - key_begin + TJ - 1) / TJ, B);
     size_t smem = sizeof(float) * ((size_t)Hkv * D + (size_t)Hkv * TJ);
