@@ -223,6 +223,88 @@ __global__ void __launch_bounds__(kSelectThreads) select_pages_kernel(const floa
     if (threadIdx.x == 0) top_count[seg] = k * P;
 }
 
+// The same selection with one warp per (b, h) segment, for tables of up to 32 * kRounds pages:
+// lane l holds the rank keys of pages l, l + 32, ... in registers.  A bitwise radix select,
+// most significant bit first, finds the k-th smallest key: at each bit, the pages that agree
+// with the bits chosen so far are counted by ballots, split by that bit; if enough of them
+// have a 0 there, the bit is 0 and those with a 1 are out, otherwise it is 1 and those with a
+// 0 are in.  The pages whose whole key equals the selected one then fill what is left, lowest
+// page index first.  The kept pages go to shared memory in page order, then out as their keys.
+constexpr int kWarpSelectWarps = 8;
+
+template <int kRounds>
+__global__ void __launch_bounds__(kWarpSelectWarps * 32) select_pages_warp_kernel(
+    const float* __restrict__ page_scores, const int32_t* __restrict__ cache_len, int B, int Hkv, int max_pages,
+    int pshift, int w, const int32_t* __restrict__ w_head, int32_t* __restrict__ top_idx,
+    int32_t* __restrict__ top_count, int top_cap, int* status)
+{
+    __shared__ int32_t kept_pages[kWarpSelectWarps][32 * kRounds];
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = blockIdx.x * kWarpSelectWarps + wid;
+    if (seg >= B * Hkv) return;  // whole warp
+    const int b = seg / Hkv;
+    const int Lmax = max_pages << pshift;
+    const int L = cache_len ? min(max(cache_len[b], 0), Lmax) : Lmax;
+    const int n_c = min(L >> pshift, max_pages);  // complete pages
+    int wb = w;
+    if (w_head) {
+        wb = w_head[seg % Hkv];
+        if (wb < 0 || wb > w) {
+            if (lane == 0) set_status(status, DMA_ERR_DEVICE_CHECK);
+            wb = wb < 0 ? 0 : w;
+        }
+    }
+    const int k = min(wb >> pshift, n_c);
+    const float* ps = page_scores + (int64_t)seg * max_pages;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t key[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int p = 32 * r + lane;
+        key[r] = p < n_c ? rank_key(ps[p]) : 0xffffffffu;
+    }
+    uint32_t sel = 0;  // the bits of the k-th smallest key chosen so far
+    int need = k;      // pages agreeing with those bits still to keep
+    if (k > 0 && k < n_c) {
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t hi = bit == 31 ? 0u : ~0u << (bit + 1);  // the bits already chosen
+            int zeros = 0;
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) {
+                const bool zero = 32 * r + lane < n_c && ((key[r] ^ sel) & hi) == 0 && ((key[r] >> bit) & 1u) == 0;
+                zeros += __popc(__ballot_sync(0xffffffffu, zero));
+            }
+            if (need > zeros) {
+                need -= zeros;
+                sel |= 1u << bit;
+            }
+        }
+    }
+    // kept: every page when k >= n_c; else a key below the selected one, or equal to it and
+    // among the first `need` such pages
+    int32_t* mine = kept_pages[wid];
+    int n_kept = 0, n_tied = 0;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+        const int p = 32 * r + lane;
+        bool kept = p < n_c && k > 0;
+        if (k < n_c) {
+            const bool tied = p < n_c && key[r] == sel;
+            const unsigned tb = __ballot_sync(0xffffffffu, tied);
+            kept = k > 0 && ((p < n_c && key[r] < sel) || (tied && n_tied + __popc(tb & lt) < need));
+            n_tied += __popc(tb);
+        }
+        const unsigned kb = __ballot_sync(0xffffffffu, kept);
+        if (kept) mine[n_kept + __popc(kb & lt)] = p;
+        n_kept += __popc(kb);
+    }
+    __syncwarp();
+    const int P = 1 << pshift;
+    int32_t* out = top_idx + (int64_t)seg * top_cap;
+    for (int t = lane; t < k * P; t += 32) out[t] = (mine[t >> pshift] << pshift) + (t & (P - 1));
+    if (lane == 0) top_count[seg] = k * P;
+}
+
 template <typename T, int D>
 cudaError_t score_paged_typed(const void* Vp, const int32_t* bt, int n_pages, int B, int max_pages, int pshift,
                               int Hkv, int key_begin, int key_end, const int32_t* cache_len, const float* W,
@@ -268,10 +350,20 @@ cudaError_t launch_select_pages(const float* page_scores, int B, int Hkv, int ma
                                 const int32_t* cache_len, int w, const int32_t* w_head, int32_t* top_idx,
                                 int32_t* top_count, int top_cap, int* status, cudaStream_t st)
 {
+    cudaError_t e = cudaSuccess;
+    if (max_pages <= 1024) {
+        const int grid = (B * Hkv + kWarpSelectWarps - 1) / kWarpSelectWarps;
+        if (max_pages <= 512)
+            select_pages_warp_kernel<16><<<grid, kWarpSelectWarps * 32, 0, st>>>(
+                page_scores, cache_len, B, Hkv, max_pages, pshift, w, w_head, top_idx, top_count, top_cap, status);
+        else
+            select_pages_warp_kernel<32><<<grid, kWarpSelectWarps * 32, 0, st>>>(
+                page_scores, cache_len, B, Hkv, max_pages, pshift, w, w_head, top_idx, top_count, top_cap, status);
+        return cudaGetLastError();
+    }
     int n = 1;
     while (n < max_pages) n <<= 1;
     const int smem = n * 8;
-    cudaError_t e = cudaSuccess;
     if (smem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(select_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
             cudaSuccess)

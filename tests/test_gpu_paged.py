@@ -199,3 +199,49 @@ def test_paged_decode_b64_l32k(dma):
     assert torch.equal(h_inp["Kc"][-1], dd["Kc"][sample[-1]].cpu())
     swapped = check_against_oracle(st, o, lse, h_inp, lens, 64, w, window, batches=sample)
     print("paged decode parity b64 l32k", dict(segments_with_near_tie_swaps=swapped))
+
+
+def _pages_by_definition(ps, n_c, k):
+    """The k best of the first n_c pages under (score descending, page index ascending), in page
+    order: Python's sort of the page scores, as fp32 values."""
+    vals = [float(np.float32(x)) for x in ps[:n_c]]
+    return sorted(sorted(range(n_c), key=lambda p: (-vals[p], p))[:k])
+
+
+@pytest.mark.parametrize("max_pages,n_levels", [(512, 2), (700, 3), (700, 1), (1024, 3), (1500, 4), (2500, 3)])
+def test_page_selection_with_exact_ties(dma, max_pages, n_levels):
+    """Page scores drawn from a few exact values (n_levels = 1: all equal), so that the cutoff
+    falls inside a run of equal scores: the kept pages are those of the definition, ties to the
+    lower page index.  Sequences of different lengths put the cutoff at different places.
+    Tables of up to 512 and up to 1024 pages take the two instantiations of the
+    one-warp-per-segment select; 1500 and 2500 pages take the one-CTA-per-segment kernel (its sort
+    above 1024 complete pages, its counting rank below).
+    Per-head budgets too: the uniform list and an uneven one with a zero budget."""
+    B, Hkv, P, w = 3, 4, 16, 16 * 300
+    gen = torch.Generator().manual_seed(90 + max_pages + n_levels)
+    levels = torch.tensor([0.25 * (1 + e) for e in range(n_levels)], dtype=torch.float32)
+    ps = levels[torch.randint(0, n_levels, (B, Hkv, max_pages), generator=gen)]
+    ps[1, 2, :] = levels[-1]  # one segment wholly tied
+    lens = [max_pages * P, (max_pages // 2) * P + 5, 301 * P]
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ps_d = ps.cuda()
+    top_cap = (w // P) * P
+    for w_head in (None, [w, w // 3, P * 7, 0]):
+        top_idx = torch.full((B, Hkv, top_cap), -7, dtype=torch.int32, device="cuda")
+        top_count = torch.full((B, Hkv), -7, dtype=torch.int32, device="cuda")
+        if w_head is None:
+            dma.dma_select_pages(ps_d, P, w, top_idx, top_count, cl)
+        else:
+            wh = torch.tensor(w_head, dtype=torch.int32, device="cuda")
+            dma.dma_select_pages_heads(ps_d, P, w, wh, top_idx, top_count, cl)
+        torch.cuda.synchronize()
+        assert dma.dma_get_device_status() == 0
+        for b in range(B):
+            n_c = min(lens[b] // P, max_pages)
+            for h in range(Hkv):
+                budget = w if w_head is None else w_head[h]
+                k = min(budget // P, n_c)
+                want = _pages_by_definition(ps[b, h].tolist(), n_c, k)
+                n = int(top_count[b, h])
+                got = top_idx[b, h, :n].cpu().tolist()
+                assert got == [p * P + e for p in want for e in range(P)], (max_pages, n_levels, w_head, b, h)
