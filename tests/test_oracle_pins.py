@@ -484,3 +484,17 @@ def test_select_pages_is_block_selection_of_the_last_row(oracle_mod, page_size):
             keys = sorted(j for p in kept[(b, h)] for j in range(p * page_size, (p + 1) * page_size))
             assert keys == sorted(top), (b, h)
             assert len(kept[(b, h)]) == min(w // page_size, L // page_size)
+
+
+def test_select_pages_cutoff_inside_exact_ties(oracle_mod):
+    """Equal page scores decide by page index alone: with every key score equal the kept pages are
+    0 .. k-1; with two score levels the higher pages all go in first and the tied lower ones
+    fill the rest from page 0 up."""
+    P, w = 16, 16 * 5
+    scores = torch.full((1, 2, 16 * 12), 0.75, dtype=torch.float64)
+    high = [3, 8]
+    for p in high:
+        scores[0, 1, p * P + 7] = 2.0  # one key raises the page's maximum
+    kept = oracle_mod.select_pages(scores, [16 * 12], P, w)
+    assert kept[(0, 0)] == [0, 1, 2, 3, 4]
+    assert kept[(0, 1)] == sorted(high + [0, 1, 2])
